@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs for sink attention.
+
+This module only draws random tensors and packs sequence offsets; it holds
+none of the attention arithmetic, so both the CUDA path and the fp64 oracle
+can take their inputs from it.
+
+The pages benchmark nothing at the kernel level: the model they train is a
+20B-class MoE LLM (page "GPT-OSS Agentic RL Training: A Practical
+Retrospective", section "Agentic RL and GPT-OSS") on GSM8K, Retool and
+VerifyIf. None of that is available, so these tensors stand in for one
+attention layer of such a model: 64 query heads over 8 key/value heads of
+width 64, bf16 activations, fp32 sinks, and for the RL rollout case a packed
+batch of sequences of uneven length (section "Scaling Memory Efficiency for
+Long Contexts": contexts grow as environment feedback is appended).
+
+Recipe (all drawn on the CPU with ``torch.Generator().manual_seed(seed)``,
+in the order lengths -> q -> k -> v -> dO -> sinks; values drawn in fp32 and
+rounded to bf16 with round-to-nearest-even):
+
+  tiny         seed 1  B=1  T=128   Hq=4  Hkv=1 causal            q,k,v,dO ~ N(0,1)   S ~ U(-2,2)
+  dense        seed 2  B=4  T=2048  Hq=64 Hkv=8 causal            N(0,1)              S ~ U(-2,2)
+  window       seed 3  as dense, causal window of 128 keys        N(0,1)              S ~ U(-4,4)
+  varlen       seed 4  32 sequences, L ~ randint[256, 8192]       N(0,1)              even heads S ~ U(-2,2),
+                       (inclusive), Hq=64 Hkv=8 causal                                odd heads S = -30
+  long         seed 5  B=1  T=32768 Hq=64 Hkv=8 causal            q,k ~ 2 N(0,1)      S ~ U(-10,10)
+                                                                  v,dO ~ N(0,1)
+  long_window  seed 5  as long, causal window of 128 keys
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+HEAD_DIM = 64
+
+
+@dataclass
+class Workload:
+    name: str
+    q: torch.Tensor          # bf16 [total, Hq, d]
+    k: torch.Tensor          # bf16 [total, Hkv, d]
+    v: torch.Tensor          # bf16 [total, Hkv, d]
+    dout: torch.Tensor       # bf16 [total, Hq, d]
+    sinks: torch.Tensor      # fp32 [Hq]
+    cu_seqlens: torch.Tensor  # int32 [nseq + 1]
+    causal: bool = True
+    window: int = 0
+    scale: float = HEAD_DIM ** -0.5
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def total(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def nseq(self) -> int:
+        return int(self.cu_seqlens.numel() - 1)
+
+    @property
+    def max_seqlen(self) -> int:
+        lens = self.cu_seqlens[1:] - self.cu_seqlens[:-1]
+        return int(lens.max()) if lens.numel() else 0
+
+    @property
+    def Hq(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def Hkv(self) -> int:
+        return int(self.k.shape[1])
+
+
+def _offsets(lengths) -> torch.Tensor:
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    if len(lengths):
+        cu[1:] = torch.cumsum(torch.as_tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    return cu
+
+
+def make(name: str, lengths, Hq: int, Hkv: int, *, seed: int, causal: bool = True,
+         window: int = 0, qk_std: float = 1.0, sink_range=(-2.0, 2.0),
+         odd_head_sink=None, d: int = HEAD_DIM, no_sink: bool = False) -> Workload:
+    """Draw one workload. ``lengths`` may be a list of ints or a callable
+    taking the generator and returning one (so lengths are drawn first)."""
+    g = torch.Generator().manual_seed(seed)
+    if callable(lengths):
+        lengths = lengths(g)
+    lengths = [int(x) for x in lengths]
+    total = sum(lengths)
+
+    def draw(h, std):
+        return (torch.randn(total, h, d, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    q = draw(Hq, qk_std)
+    k = draw(Hkv, qk_std)
+    v = draw(Hkv, 1.0)
+    dout = draw(Hq, 1.0)
+    lo, hi = sink_range
+    sinks = torch.rand(Hq, generator=g, dtype=torch.float32) * (hi - lo) + lo
+    if odd_head_sink is not None:
+        sinks[1::2] = odd_head_sink
+    meta = {"lengths": lengths, "seed": seed, "no_sink": no_sink}
+    return Workload(name, q, k, v, dout, sinks, _offsets(lengths), causal, window,
+                    d ** -0.5, meta)
+
+
+def _varlen_lengths(g):
+    return torch.randint(256, 8192 + 1, (32,), generator=g).tolist()
+
+
+CONFIGS = {
+    "tiny": dict(lengths=[128], Hq=4, Hkv=1, seed=1),
+    "dense": dict(lengths=[2048] * 4, Hq=64, Hkv=8, seed=2),
+    "window": dict(lengths=[2048] * 4, Hq=64, Hkv=8, seed=3, window=128, sink_range=(-4.0, 4.0)),
+    "varlen": dict(lengths=_varlen_lengths, Hq=64, Hkv=8, seed=4, odd_head_sink=-30.0),
+    "long": dict(lengths=[32768], Hq=64, Hkv=8, seed=5, qk_std=2.0, sink_range=(-10.0, 10.0)),
+    "long_window": dict(lengths=[32768], Hq=64, Hkv=8, seed=5, qk_std=2.0,
+                        sink_range=(-10.0, 10.0), window=128),
+}
+
+# One-line descriptions, used in reports.
+DESCRIPTIONS = {
+    "tiny": "B=1 T=128 Hq=4 Hkv=1 d=64 causal",
+    "dense": "B=4 T=2048 Hq=64 Hkv=8 d=64 causal",
+    "window": "B=4 T=2048 Hq=64 Hkv=8 d=64 causal window=128",
+    "varlen": "32 packed seqs L~U[256,8192] Hq=64 Hkv=8 d=64 causal, odd-head sinks -30",
+    "long": "B=1 T=32768 Hq=64 Hkv=8 d=64 causal, q,k~2N(0,1), S~U(-10,10)",
+    "long_window": "B=1 T=32768 Hq=64 Hkv=8 d=64 causal window=128, q,k~2N(0,1)",
+}
+
+
+def config(name: str) -> Workload:
+    return make(name, **CONFIGS[name])
