@@ -1,0 +1,172 @@
+"""Torch-facing entry points: ``forward``, ``backward`` and the autograd op
+``sink_attention``. PyTorch supplies device memory and the stream; the work
+is done by libsinkattn.so through its C ABI (argument marshalling only).
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _binding
+from ._binding import BwdParams, FwdParams, check
+
+HEAD_DIM = 64
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _events(evs) -> Sequence[Optional[int]]:
+    if evs is None:
+        return (None, None)
+    out = []
+    for e in evs:
+        h = e.cuda_event if e is not None else 0
+        out.append(h or None)
+    return out
+
+
+def _check_tokens(name: str, t: torch.Tensor, heads_dim: int):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3:
+        raise ValueError(f"{name} must be a bf16 CUDA tensor [total, heads, 64]")
+    if t.shape[2] != HEAD_DIM or t.stride(2) != 1 or t.stride(1) != HEAD_DIM:
+        raise ValueError(f"{name}: heads and features must be contiguous (strides (*, 64, 1))")
+
+
+def _fill_fwd(p: FwdParams, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale, o, lse):
+    total, Hq, d = q.shape
+    p.q, p.k, p.v = _ptr(q), _ptr(k), _ptr(v)
+    p.sinks = _ptr(sinks)
+    p.cu_seqlens = _ptr(cu_seqlens)
+    p.o, p.lse = _ptr(o), _ptr(lse)
+    p.q_row_stride, p.k_row_stride, p.v_row_stride = q.stride(0), k.stride(0), v.stride(0)
+    p.nseq = cu_seqlens.numel() - 1
+    p.total = total
+    p.max_seqlen = int(max_seqlen)
+    p.Hq, p.Hkv, p.head_dim = Hq, k.shape[1], d
+    p.causal = 1 if causal else 0
+    p.window = int(window)
+    p.softmax_scale = float(scale) if scale is not None else 0.0
+
+
+def _validate_inputs(q, k, v, sinks, cu_seqlens):
+    _check_tokens("q", q, 1)
+    _check_tokens("k", k, 1)
+    _check_tokens("v", v, 1)
+    if k.shape != v.shape or k.shape[0] != q.shape[0]:
+        raise ValueError("k and v must be [total, Hkv, 64] with the same total as q")
+    if sinks is not None and (sinks.dtype != torch.float32 or not sinks.is_cuda or
+                              sinks.shape != (q.shape[1],) or not sinks.is_contiguous()):
+        raise ValueError("sinks must be a contiguous fp32 CUDA tensor [Hq]")
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be an int32 CUDA tensor [nseq + 1]")
+
+
+def forward(q, k, v, sinks, cu_seqlens, max_seqlen, *, causal=True, window=0, scale=None,
+            out=None, lse=None, workspace=None, timing_events=None):
+    """O [total, Hq, 64] bf16 and LSE [Hq, total] fp32 (natural log)."""
+    _validate_inputs(q, k, v, sinks, cu_seqlens)
+    L = _binding.lib()
+    total, Hq, d = q.shape
+    nseq = cu_seqlens.numel() - 1
+    o = out if out is not None else torch.empty(total, Hq, d, dtype=torch.bfloat16, device=q.device)
+    lse = lse if lse is not None else torch.empty(Hq, total, dtype=torch.float32, device=q.device)
+    nbytes = L.sinkattn_fwd_workspace_size(nseq, total, Hq, k.shape[1], d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    p = FwdParams()
+    _fill_fwd(p, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale, o, lse)
+    p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
+    p.timing_events[0], p.timing_events[1] = _events(timing_events)
+    check(L.sinkattn_fwd(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_fwd")
+    return o, lse
+
+
+def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=True, window=0,
+             scale=None, dq=None, dk=None, dv=None, dsinks=None, workspace=None,
+             timing_events=None):
+    """dq, dk, dv (bf16, shaped like q, k, v but contiguous) and dsinks [Hq]
+    fp32 (None when ``sinks`` is None)."""
+    _validate_inputs(q, k, v, sinks, cu_seqlens)
+    for name, t in (("o", o), ("dout", dout)):
+        _check_tokens(name, t, 1)
+        if not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError(f"{name} must be contiguous and shaped like q")
+    L = _binding.lib()
+    total, Hq, d = q.shape
+    Hkv = k.shape[1]
+    nseq = cu_seqlens.numel() - 1
+    dq = dq if dq is not None else torch.empty(total, Hq, d, dtype=torch.bfloat16, device=q.device)
+    dk = dk if dk is not None else torch.empty(total, Hkv, d, dtype=torch.bfloat16, device=q.device)
+    dv = dv if dv is not None else torch.empty(total, Hkv, d, dtype=torch.bfloat16, device=q.device)
+    if sinks is not None and dsinks is None:
+        dsinks = torch.empty(Hq, dtype=torch.float32, device=q.device)
+    nbytes = L.sinkattn_bwd_workspace_size(nseq, total, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    p = BwdParams()
+    _fill_fwd(p.fwd, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale, o, lse)
+    p.dout, p.dq, p.dk, p.dv = _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv)
+    p.dsinks = _ptr(dsinks)
+    p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
+    p.timing_events[0], p.timing_events[1] = _events(timing_events)
+    check(L.sinkattn_bwd(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_bwd")
+    return dq, dk, dv, dsinks
+
+
+def workspace_bytes(kind: str, nseq: int, total: int, Hq: int, Hkv: int) -> int:
+    L = _binding.lib()
+    fn = L.sinkattn_fwd_workspace_size if kind == "fwd" else L.sinkattn_bwd_workspace_size
+    return int(fn(nseq, total, Hq, Hkv, HEAD_DIM))
+
+
+class _SinkAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale):
+        o, lse = forward(q, k, v, sinks, cu_seqlens, max_seqlen, causal=causal, window=window,
+                         scale=scale)
+        ctx.save_for_backward(q, k, v, sinks, cu_seqlens, o, lse)
+        ctx.args = (max_seqlen, causal, window, scale)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, sinks, cu_seqlens, o, lse = ctx.saved_tensors
+        max_seqlen, causal, window, scale = ctx.args
+        dq, dk, dv, ds = backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse,
+                                  do.contiguous(), causal=causal, window=window, scale=scale)
+        return dq, dk, dv, ds, None, None, None, None, None
+
+
+def sink_attention(q, k, v, sinks=None, cu_seqlens=None, max_seqlen=None, *, causal=True,
+                   window=0, scale=None):
+    """Attention with one learnable sink logit per query head.
+
+    q [total, Hq, 64], k/v [total, Hkv, 64] bf16 with cu_seqlens (int32
+    [nseq+1]) for packed variable-length batches, or q [B, T, Hq, 64],
+    k/v [B, T, Hkv, 64] for a dense batch. sinks: fp32 [Hq] or None.
+    Returns O shaped like q. Differentiable in q, k, v and sinks.
+    """
+    batched = q.dim() == 4
+    if batched:
+        B, T = q.shape[:2]
+        q, k, v = (x.reshape(B * T, *x.shape[2:]) for x in (q, k, v))
+        if cu_seqlens is None:
+            cu_seqlens = torch.arange(0, (B + 1) * T, T, dtype=torch.int32, device=q.device)
+            max_seqlen = T
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, q.shape[0]], dtype=torch.int32, device=q.device)
+        max_seqlen = q.shape[0]
+    if max_seqlen is None:
+        lens = cu_seqlens[1:] - cu_seqlens[:-1]
+        max_seqlen = int(lens.max().item()) if lens.numel() else 0
+    o = _SinkAttention.apply(q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale)
+    return o.reshape(B, T, *o.shape[1:]) if batched else o

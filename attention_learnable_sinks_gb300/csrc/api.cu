@@ -1,0 +1,301 @@
+// C ABI of libsinkattn.so (declared in include/sinkattn.h): argument checks,
+// workspace layout and the order of kernel launches. No device memory is
+// allocated here; every buffer, workspace included, belongs to the caller.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/sinkattn.h"
+#include "internal.h"
+
+namespace sinkattn {
+
+namespace {
+
+__device__ int32_t g_error_word;  // first error recorded by any kernel
+
+std::atomic<uint64_t> g_launches{0};
+thread_local std::string g_message;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int32_t* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+sinkattn_status fail(sinkattn_status st, const std::string& msg) {
+  g_message = msg;
+  return st;
+}
+
+// Per-device constants: address of the error word, SM count.
+sinkattn_status device_info(int32_t** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SINKATTN_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(SINKATTN_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_error_word);
+    if (e != cudaSuccess)
+      return fail(SINKATTN_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+      return fail(SINKATTN_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(SINKATTN_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300) only");
+    g_err_ptr[dev] = static_cast<int32_t*>(ptr);
+    g_num_sms[dev] = n;
+  }
+  *err = g_err_ptr[dev];
+  *sms = g_num_sms[dev];
+  return SINKATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Workspace layout. Forward: [meta | q-tile items]. Backward:
+// [meta | q-tile items | meta | k-tile items | D | sink partials | dq_acc].
+struct Layout {
+  size_t q_meta, q_items, k_meta, k_items, D, part, dq_acc, bytes;
+  int32_t capacity, nchunks;
+};
+
+Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
+  Layout l{};
+  l.capacity = tile_capacity(nseq, total);
+  l.nchunks = (total + kTile - 1) / kTile;
+  size_t off = 0;
+  l.q_meta = off;
+  off += 256;
+  l.q_items = off;
+  off += align256(sizeof(int2) * (size_t)l.capacity);
+  if (bwd) {
+    l.k_meta = off;
+    off += 256;
+    l.k_items = off;
+    off += align256(sizeof(int2) * (size_t)l.capacity);
+    l.D = off;
+    off += align256(sizeof(float) * (size_t)Hq * total);
+    l.part = off;
+    off += align256(sizeof(float) * (size_t)Hq * l.nchunks);
+    l.dq_acc = off;
+    off += align256(sizeof(float) * (size_t)total * Hq * kHeadDim);
+  }
+  l.bytes = off;
+  return l;
+}
+
+bool shape_ok(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv) {
+  return nseq >= 0 && total >= 0 && Hq > 0 && Hkv > 0 && Hq % Hkv == 0 && Hq <= 65535;
+}
+
+// Checks shared by forward and backward; fills the kernels' view.
+sinkattn_status check_fwd(const sinkattn_fwd_params* a, Problem* p) {
+  if (!a) return fail(SINKATTN_ERR_INVALID_ARG, "params is NULL");
+  if (a->head_dim != kHeadDim)
+    return fail(SINKATTN_ERR_UNSUPPORTED, "head_dim must be 64");
+  if (!shape_ok(a->nseq, a->total, a->Hq, a->Hkv))
+    return fail(SINKATTN_ERR_INVALID_ARG, "need nseq >= 0, total >= 0, 0 < Hkv, Hq % Hkv == 0, Hq <= 65535");
+  if (a->causal != 0 && a->causal != 1) return fail(SINKATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (a->window > 0 && !a->causal)
+    return fail(SINKATTN_ERR_UNSUPPORTED, "a sliding window needs causal = 1");
+  if (a->max_seqlen < 0 || (a->total > 0 && a->max_seqlen < 1))
+    return fail(SINKATTN_ERR_INVALID_ARG, "max_seqlen must be >= 1 (>= 0 when total is 0)");
+  if (!a->cu_seqlens) return fail(SINKATTN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (std::isnan(a->softmax_scale) || std::isinf(a->softmax_scale))
+    return fail(SINKATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
+  const int64_t qs = a->q_row_stride ? a->q_row_stride : (int64_t)a->Hq * kHeadDim;
+  const int64_t ks = a->k_row_stride ? a->k_row_stride : (int64_t)a->Hkv * kHeadDim;
+  const int64_t vs = a->v_row_stride ? a->v_row_stride : (int64_t)a->Hkv * kHeadDim;
+  if (qs < (int64_t)a->Hq * kHeadDim || ks < (int64_t)a->Hkv * kHeadDim || vs < (int64_t)a->Hkv * kHeadDim ||
+      qs % 8 || ks % 8 || vs % 8)
+    return fail(SINKATTN_ERR_INVALID_ARG, "row strides must cover all heads and be multiples of 8 elements");
+  if (a->total > 0) {
+    if (!a->q || !a->k || !a->v || !a->o) return fail(SINKATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o) ||
+        (a->lse && !aligned16(a->lse)))
+      return fail(SINKATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  }
+  p->q = static_cast<const __nv_bfloat16*>(a->q);
+  p->k = static_cast<const __nv_bfloat16*>(a->k);
+  p->v = static_cast<const __nv_bfloat16*>(a->v);
+  p->sinks = a->sinks;
+  p->cu = a->cu_seqlens;
+  p->o = static_cast<__nv_bfloat16*>(a->o);
+  p->lse = a->lse;
+  p->q_stride = qs;
+  p->k_stride = ks;
+  p->v_stride = vs;
+  p->nseq = a->nseq;
+  p->total = a->total;
+  p->max_seqlen = a->max_seqlen;
+  p->Hq = a->Hq;
+  p->Hkv = a->Hkv;
+  p->G = a->Hq / a->Hkv;
+  p->causal = a->causal;
+  p->window = a->window > 0 ? a->window : 0;
+  p->scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+  p->scale_log2 = p->scale * 1.4426950408889634f;
+  return SINKATTN_OK;
+}
+
+sinkattn_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(SINKATTN_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+void record(void* ev, cudaStream_t s) {
+  if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
+}  // namespace
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace sinkattn
+
+using namespace sinkattn;
+
+extern "C" {
+
+size_t sinkattn_fwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
+                                   int32_t head_dim) {
+  if (!shape_ok(nseq, total, Hq, Hkv) || head_dim != kHeadDim) return 0;
+  return layout(nseq, total, Hq, false).bytes;
+}
+
+size_t sinkattn_bwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
+                                   int32_t head_dim) {
+  if (!shape_ok(nseq, total, Hq, Hkv) || head_dim != kHeadDim) return 0;
+  return layout(nseq, total, Hq, true).bytes;
+}
+
+sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
+  g_message.clear();
+  Problem p{};
+  sinkattn_status st = check_fwd(a, &p);
+  if (st != SINKATTN_OK) return st;
+  const Layout l = layout(a->nseq, a->total, a->Hq, false);
+  if (!a->workspace || a->workspace_bytes < l.bytes)
+    return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_fwd_workspace_size()");
+  if (a->total == 0) return SINKATTN_OK;
+  int sms = 0;
+  st = device_info(&p.err, &sms);
+  if (st != SINKATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(a->workspace);
+  TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
+              l.capacity};
+  cudaError_t e = launch_build_tile_list(p, 0, qt, s);
+  if (e != cudaSuccess) return cuda_fail(e, "tile list");
+  record(a->timing_events[0], s);
+  e = launch_fwd(p, qt, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "forward kernel");
+  record(a->timing_events[1], s);
+  return SINKATTN_OK;
+}
+
+sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
+  g_message.clear();
+  if (!a) return fail(SINKATTN_ERR_INVALID_ARG, "params is NULL");
+  BwdProblem bp{};
+  sinkattn_status st = check_fwd(&a->fwd, &bp.f);
+  if (st != SINKATTN_OK) return st;
+  const sinkattn_fwd_params& f = a->fwd;
+  if (f.total > 0) {
+    if (!f.lse || !a->dout || !a->dq || !a->dk || !a->dv)
+      return fail(SINKATTN_ERR_INVALID_ARG, "lse, dout, dq, dk and dv must be non-NULL");
+    if (!aligned16(a->dout) || !aligned16(a->dq) || !aligned16(a->dk) || !aligned16(a->dv))
+      return fail(SINKATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  }
+  const Layout l = layout(f.nseq, f.total, f.Hq, true);
+  if (!a->workspace || a->workspace_bytes < l.bytes)
+    return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_bwd_workspace_size()");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (f.total == 0) {
+    if (a->dsinks) {
+      cudaError_t e = cudaMemsetAsync(a->dsinks, 0, sizeof(float) * f.Hq, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dsinks clear");
+    }
+    return SINKATTN_OK;
+  }
+  int sms = 0;
+  st = device_info(&bp.f.err, &sms);
+  if (st != SINKATTN_OK) return st;
+  char* ws = static_cast<char*>(a->workspace);
+  bp.dout = static_cast<const __nv_bfloat16*>(a->dout);
+  bp.dq = static_cast<__nv_bfloat16*>(a->dq);
+  bp.dk = static_cast<__nv_bfloat16*>(a->dk);
+  bp.dv = static_cast<__nv_bfloat16*>(a->dv);
+  bp.dsinks = a->dsinks;
+  bp.D = reinterpret_cast<float*>(ws + l.D);
+  bp.sink_part = reinterpret_cast<float*>(ws + l.part);
+  bp.dq_acc = reinterpret_cast<float*>(ws + l.dq_acc);
+  bp.nchunks = l.nchunks;
+  TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
+              l.capacity};
+  TileList kt{reinterpret_cast<int32_t*>(ws + l.k_meta), reinterpret_cast<int2*>(ws + l.k_items),
+              l.capacity};
+  cudaError_t e = launch_build_tile_list(bp.f, 0, qt, s);
+  if (e == cudaSuccess) e = launch_build_tile_list(bp.f, 1, kt, s);
+  if (e != cudaSuccess) return cuda_fail(e, "tile lists");
+  e = launch_bwd_preprocess(bp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess");
+  record(a->timing_events[0], s);
+  e = launch_bwd_dq(bp, qt, sms, s);
+  if (e == cudaSuccess) e = launch_bwd_dkdv(bp, kt, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward main");
+  record(a->timing_events[1], s);
+  e = launch_bwd_finish(bp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sink gradient reduction");
+  return SINKATTN_OK;
+}
+
+const char* sinkattn_status_string(int32_t status) {
+  switch (status) {
+    case SINKATTN_OK: return "ok";
+    case SINKATTN_ERR_INVALID_ARG: return "invalid argument";
+    case SINKATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SINKATTN_ERR_CUDA: return "CUDA error";
+    case SINKATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case SINKATTN_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    default: return "unknown status";
+  }
+}
+
+const char* sinkattn_last_error_message(void) { return g_message.c_str(); }
+
+int32_t sinkattn_device_error(int32_t reset) {
+  int32_t* err = nullptr;
+  int sms = 0;
+  if (device_info(&err, &sms) != SINKATTN_OK) return SINKATTN_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SINKATTN_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SINKATTN_ERR_CUDA;
+  if (reset) {
+    const int32_t zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return SINKATTN_ERR_CUDA;
+  }
+  return word;
+}
+
+uint64_t sinkattn_launch_count(void) { return g_launches.load(); }
+
+size_t sinkattn_params_size(int32_t which) {
+  if (which == 0) return sizeof(sinkattn_fwd_params);
+  if (which == 1) return sizeof(sinkattn_bwd_params);
+  return 0;
+}
+
+}  // extern "C"

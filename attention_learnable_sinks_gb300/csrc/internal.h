@@ -1,0 +1,87 @@
+// Internal declarations shared by the translation units of libsinkattn.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace sinkattn {
+
+constexpr int kHeadDim = 64;
+constexpr int kTile = 128;  // rows per query tile and keys per key tile
+
+// One problem as the kernels see it. Strides are in elements per token row.
+struct Problem {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* sinks;          // null: no sink
+  const int32_t* cu;           // device cu_seqlens
+  __nv_bfloat16* o;
+  float* lse;                  // [Hq, total]
+  int64_t q_stride, k_stride, v_stride;
+  int32_t nseq, total, max_seqlen, Hq, Hkv, G, causal, window;
+  float scale;                 // softmax scale
+  float scale_log2;            // scale * log2(e)
+  int32_t* err;                // device error word
+};
+
+struct BwdProblem {
+  Problem f;
+  const __nv_bfloat16* dout;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dsinks;
+  float* D;                    // [Hq, total] workspace: rowsum(dO * O)
+  float* sink_part;            // [Hq, nchunks] workspace
+  float* dq_acc;               // [total, Hq, 64] fp32 workspace
+  int32_t nchunks;             // token chunks of the preprocess pass
+};
+
+// Tile work list in the workspace: meta[0] = number of items, meta[1] = the
+// next item to hand out (work stealing), items[] = {sequence, tile} sorted by
+// decreasing cost.
+struct TileList {
+  int32_t* meta;
+  int2* items;
+  int32_t capacity;
+};
+
+// Upper bound on the number of 128-row (or 128-key) tiles of a packing.
+inline int32_t tile_capacity(int32_t nseq, int32_t total) {
+  return (total + kTile - 1) / kTile + nseq;
+}
+
+// Keys visible from any row in [r0, r1) of a sequence of length L.
+__host__ __device__ inline void visible_keys(int causal, int window, int L, int r0, int r1,
+                                             int* lo, int* hi) {
+  *hi = causal ? (r1 < L ? r1 : L) : L;
+  int l = window > 0 ? r0 - window + 1 : 0;
+  *lo = l > 0 ? l : 0;
+}
+
+// Rows that see any key in [c0, c1) of a sequence of length L.
+__host__ __device__ inline void seeing_rows(int causal, int window, int L, int c0, int c1,
+                                            int* lo, int* hi) {
+  *lo = causal ? c0 : 0;
+  int h = window > 0 ? c1 - 1 + window : L;
+  *hi = h < L ? h : L;
+}
+
+// Launchers (each returns the cudaGetLastError() of its launch).
+cudaError_t launch_build_tile_list(const Problem& p, int by_keys, const TileList& list,
+                                   cudaStream_t s);
+cudaError_t launch_fwd(const Problem& p, const TileList& qtiles, int num_sms, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdProblem& p, const TileList& qtiles, int num_sms,
+                          cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdProblem& p, const TileList& ktiles, int num_sms,
+                            cudaStream_t s);
+cudaError_t launch_bwd_finish(const BwdProblem& p, cudaStream_t s);
+
+// Counts kernel launches (sinkattn_launch_count).
+void note_launch(int n = 1);
+
+}  // namespace sinkattn

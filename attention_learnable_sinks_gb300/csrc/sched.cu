@@ -1,0 +1,139 @@
+// Varlen tile scheduler: builds, on the device, the list of 128-row query
+// tiles (forward) or 128-key key tiles (backward) of a packed batch, ordered by
+// decreasing cost so that persistent CTAs taking items in order approximate a
+// longest-processing-time-first schedule. Building on the device keeps the
+// whole call asynchronous (no host copy of cu_seqlens, no stream sync).
+//
+// Cost of a query tile = number of key tiles it sees; cost of a key tile =
+// number of query tiles that see it. Both follow from the causal / window
+// mask and the sequence length.
+#include "internal.h"
+
+namespace sinkattn {
+namespace {
+
+constexpr int kBuckets = 4096;   // cost buckets; larger costs share the last
+constexpr int kThreads = 1024;
+
+__device__ inline int tile_cost(int by_keys, int causal, int window, int L, int t) {
+  const int a = t * kTile;
+  const int b = min(L, a + kTile);
+  int lo, hi;
+  if (by_keys)
+    seeing_rows(causal, window, L, a, b, &lo, &hi);
+  else
+    visible_keys(causal, window, L, a, b, &lo, &hi);
+  if (hi <= lo) return 0;
+  return (hi + kTile - 1) / kTile - lo / kTile;
+}
+
+__global__ void __launch_bounds__(kThreads)
+build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int max_seqlen,
+                       int causal, int window, int by_keys, int capacity,
+                       int2* __restrict__ items, int32_t* __restrict__ meta,
+                       int32_t* __restrict__ err) {
+  __shared__ int hist[kBuckets];
+  __shared__ int warp_sums[kThreads / 32];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kBuckets; i += kThreads) hist[i] = 0;
+  if (tid == 0) bad = (nseq >= 0 && (cu[0] != 0 || cu[nseq] != total)) ? 1 : 0;
+  __syncthreads();
+
+  // pass 1: validate lengths, histogram of costs
+  for (int b = tid; b < nseq; b += kThreads) {
+    const int L = cu[b + 1] - cu[b];
+    if (L < 0 || L > max_seqlen) {
+      atomicOr(&bad, 1);
+      continue;
+    }
+    const int nt = (L + kTile - 1) / kTile;
+    for (int t = 0; t < nt; ++t)
+      atomicAdd(&hist[min(tile_cost(by_keys, causal, window, L, t), kBuckets - 1)], 1);
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      meta[0] = 0;
+      meta[1] = 0;
+      atomicCAS(err, 0, 1 /* SINKATTN_ERR_INVALID_ARG */);
+    }
+    return;
+  }
+
+  // exclusive scan in order of decreasing cost: thread t owns the four
+  // buckets kBuckets-1-4t ... kBuckets-4-4t
+  constexpr int kPer = kBuckets / kThreads;
+  int local[kPer];
+  int sum = 0;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    local[e] = hist[kBuckets - 1 - (tid * kPer + e)];
+    sum += local[e];
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += y;
+    }
+    warp_sums[lane] = wi - w;  // exclusive prefix of the warps
+  }
+  __syncthreads();
+  int run = warp_sums[warp] + incl - sum;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    hist[kBuckets - 1 - (tid * kPer + e)] = run;  // start offset of the bucket
+    run += local[e];
+  }
+  __shared__ int n_items;
+  if (tid == kThreads - 1) n_items = run;
+  __syncthreads();
+  if (n_items > capacity) {
+    if (tid == 0) {
+      meta[0] = 0;
+      meta[1] = 0;
+      atomicCAS(err, 0, 4 /* SINKATTN_ERR_WORKSPACE */);
+    }
+    return;
+  }
+
+  // pass 2: scatter items into their buckets (order inside a bucket is free)
+  for (int b = tid; b < nseq; b += kThreads) {
+    const int L = cu[b + 1] - cu[b];
+    const int nt = (L + kTile - 1) / kTile;
+    for (int t = 0; t < nt; ++t) {
+      const int c = min(tile_cost(by_keys, causal, window, L, t), kBuckets - 1);
+      const int pos = atomicAdd(&hist[c], 1);
+      items[pos] = make_int2(b, t);
+    }
+  }
+  if (tid == 0) {
+    meta[0] = n_items;
+    meta[1] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_tile_list(const Problem& p, int by_keys, const TileList& list,
+                                   cudaStream_t s) {
+  build_tile_list_kernel<<<1, kThreads, 0, s>>>(p.cu, p.nseq, p.total, p.max_seqlen, p.causal,
+                                                p.window, by_keys, list.capacity, list.items,
+                                                list.meta, p.err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace sinkattn

@@ -1,0 +1,442 @@
+"""Benchmark: sink-attention forward + backward on one GB300 (or N, weakly
+scaled), reported as algorithmic bf16 TFLOP/s and as a fraction of the
+measured dense bf16 tensor peak.
+
+A step is one forward and one backward (every kernel of the path) over one
+batch of the dense workload: B=4, T=2048, Hq=64, Hkv=8, d=64, causal, sinks
+~ U(-2, 2), seeded synthetic bf16 tensors. FLOPs count only the (row, key)
+pairs the mask allows: forward 4*d per pair and head, backward 10*d
+(five products), so a step is 14*d*N_pairs*Hq.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload dense|window|varlen|long|long_window|tiny]
+
+For N > 1 launch under torch.distributed.run: every rank runs its own batch
+(no collective on the data path), timing is the max over ranks, and value is
+the total over ranks. --impl reference times the fp64 CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "sink-attn fwd+bwd bf16 TFLOP/s on 1 GB300 and % of dense tensor peak"
+UNIT = "TFLOP/s"
+HEAD_DIM = 64
+L2_FLUSH_BYTES = 512 << 20          # > 126 MB L2, written between timed steps
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+THROTTLE = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+# ----------------------------------------------------------------- counting
+def allowed_pairs(lengths, causal: bool, window: int) -> int:
+    """Number of (row, key) pairs the mask allows, summed over sequences."""
+    n = 0
+    for L in lengths:
+        L = int(L)
+        if not causal:
+            n += L * L
+        elif window <= 0 or window >= L:
+            n += L * (L + 1) // 2
+        else:
+            W = window
+            n += W * (W + 1) // 2 + (L - W) * W
+    return n
+
+
+def step_flops(lengths, Hq, causal, window):
+    pairs = allowed_pairs(lengths, causal, window)
+    return 4 * HEAD_DIM * pairs * Hq, 10 * HEAD_DIM * pairs * Hq
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel_file: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, valid only while the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    src = os.path.join(ROOT, "attention_learnable_sinks_gb300", "csrc", kernel_file)
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    entry = rec.get(kernel_file)
+    if not entry or entry.get("source_sha") != sha:
+        return None
+    return entry
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(THROTTLE, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- dist
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks (every rank gets it)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- oracle leg
+ORACLE_SAMPLE = {"kv_groups": [0, 1], "seqs": [0, 1, 2, 3], "prefix": None}
+
+
+def oracle_sample_run(w, kv_groups, seqs, prefix=None):
+    """Time the fp64 oracle (as it stands) on complete GQA groups of whole
+    sequences (or their first `prefix` tokens). Returns (seconds, flops)."""
+    import oracle
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    G = w.Hq // w.Hkv
+    qh = np.concatenate([np.arange(g * G, (g + 1) * G) for g in kv_groups])
+    tok, lens = [], []
+    for b in seqs:
+        a, e = int(cu[b]), int(cu[b + 1])
+        if prefix is not None:
+            e = min(e, a + prefix)
+        tok.append(np.arange(a, e))
+        lens.append(e - a)
+    tok = np.concatenate(tok)
+    sub_cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+
+    def f64(t):
+        return t.float().numpy().astype(np.float64)
+
+    q, k, v = f64(w.q[tok][:, qh]), f64(w.k[tok][:, kv_groups]), f64(w.v[tok][:, kv_groups])
+    do = f64(w.dout[tok][:, qh])
+    s = w.sinks.numpy().astype(np.float64)[qh]
+    t0 = time.perf_counter()
+    oracle.sinkattn(q, k, v, s, sub_cu, causal=w.causal, window=w.window, scale=w.scale,
+                    dout=do, want=("o", "lse", "dq", "dk", "dv", "dsinks"))
+    dt = time.perf_counter() - t0
+    f, b = step_flops(lens, len(qh), w.causal, w.window)
+    return dt, f + b
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from attention_learnable_sinks_gb300 import workloads
+    oracle.build()
+    w = workloads.config(args.workload)
+    # bounded per-step sample: one GQA group, first sequence, first 768 tokens
+    sample = {"kv_groups": [0], "seqs": [0], "prefix": min(768, w.max_seqlen)}
+    for _ in range(args.warmup):
+        oracle_sample_run(w, **sample)
+    secs, flops = 0.0, 0
+    for _ in range(args.steps):
+        dt, f = oracle_sample_run(w, **sample)
+        secs += dt
+        flops += f
+    value = flops / secs / 1e12
+    cores = oracle.default_threads()
+    desc = (f"fp64 oracle, kv group 0 ({w.Hq // w.Hkv} query heads), sequence 0, first "
+            f"{sample['prefix']} tokens of {args.workload}, fwd+bwd per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": workload_config(w, args.workload),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, name):
+    from attention_learnable_sinks_gb300.workloads import DESCRIPTIONS
+    return {"workload": f"{name}: {DESCRIPTIONS[name]}", "nseq": w.nseq, "total_tokens": w.total,
+            "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": HEAD_DIM, "causal": w.causal,
+            "window": w.window, "l2": "flushed between timed steps (512 MiB write)",
+            "flop_convention": "14*d*N_allowed_pairs*Hq (fwd 4*d, bwd 10*d)"}
+
+
+# ----------------------------------------------------------------- gb300 leg
+def run_gb300(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    from attention_learnable_sinks_gb300 import _binding, api, workloads
+    _binding.lib()
+    w = workloads.config(args.workload)
+    lengths = w.meta["lengths"]
+    fwd_flops, bwd_flops = step_flops(lengths, w.Hq, w.causal, w.window)
+    flops = fwd_flops + bwd_flops
+
+    q, k, v, do = (t.to(device) for t in (w.q, w.k, w.v, w.dout))
+    s, cu = w.sinks.to(device), w.cu_seqlens.to(device)
+    maxlen = w.max_seqlen
+    total, Hq, Hkv = w.total, w.Hq, w.Hkv
+    o = torch.empty(total, Hq, HEAD_DIM, dtype=torch.bfloat16, device=device)
+    lse = torch.empty(Hq, total, dtype=torch.float32, device=device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ds = torch.empty(Hq, dtype=torch.float32, device=device)
+    ws_f = torch.empty(api.workspace_bytes("fwd", w.nseq, total, Hq, Hkv), dtype=torch.uint8,
+                       device=device)
+    ws_b = torch.empty(api.workspace_bytes("bwd", w.nseq, total, Hq, Hkv), dtype=torch.uint8,
+                       device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record()  # creates the CUDA event so the library can record into it
+        return evs
+
+    K = args.steps
+    step_ev = [new_events(2) for _ in range(K)]
+    fwd_ev = [new_events(2) for _ in range(K)]
+    bwd_ev = [new_events(2) for _ in range(K)]
+
+    def step(i=None):
+        api.forward(q, k, v, s, cu, maxlen, causal=w.causal, window=w.window, scale=w.scale,
+                    out=o, lse=lse, workspace=ws_f,
+                    timing_events=None if i is None else fwd_ev[i])
+        api.backward(q, k, v, s, cu, maxlen, o, lse, do, causal=w.causal, window=w.window,
+                     scale=w.scale, dq=dq, dk=dk, dv=dv, dsinks=ds, workspace=ws_b,
+                     timing_events=None if i is None else bwd_ev[i])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert _binding.device_error() == 0, "device error word set during warm-up"
+
+    props = torch.cuda.get_device_properties(device)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    n0 = _binding.launch_count()
+    for i in range(K):
+        flush.zero_()
+        step_ev[i][0].record()
+        step(i)
+        step_ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = _binding.launch_count() - n0
+    clk = clocks.stop()
+    assert _binding.device_error() == 0, "device error word set during the timed region"
+
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    bwd_ms = [a.elapsed_time(b) for a, b in bwd_ev]
+    total_ms = reduce_max(sum(step_ms), world, device)
+    ms_per_step = total_ms / K
+    value = flops * world * K / (total_ms / 1e3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    hq, hk, hv, hdo = (t.pin_memory() for t in (w.q, w.k, w.v, w.dout))
+    hs, hcu = w.sinks.pin_memory(), w.cu_seqlens.pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+    hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
+    hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
+    hds = torch.empty(ds.shape, dtype=ds.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hs, hcu))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv, hds))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        s.copy_(hs, non_blocking=True)
+        cu.copy_(hcu, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+        hds.copy_(ds, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [new_events(2) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        e2e_ev[i][0].record()
+        e2e_step()
+        e2e_ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_total = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, device)
+    e2e_value = flops * world * K / (e2e_total / 1e3) / 1e12
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    f_avg, b_avg = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    if b_avg >= f_avg:
+        dom, dom_ms, dom_flops, dom_file = "bwd main", b_avg, bwd_flops, "bwd.cu"
+    else:
+        dom, dom_ms, dom_flops, dom_file = "fwd", f_avg, fwd_flops, "fwd.cu"
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    tr = traffic_record(dom_file)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16 dense (burst)",
+                "traffic": tr["dram_bytes_per_launch"] if tr else None}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": workload_config(w, args.workload),
+        "frac_of_peak": value / world / peak, "peak_tflops": peak, "peak_source": peak_src,
+        "fwd_ms": f_avg, "bwd_main_ms": b_avg,
+        "fwd_tflops": fwd_flops / (f_avg / 1e3) / 1e12,
+        "bwd_main_tflops": bwd_flops / (b_avg / 1e3) / 1e12,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, f = oracle_sample_run(w, **ORACLE_SAMPLE)
+        import oracle
+        line["cpu_baseline"] = {
+            "value": f / secs / 1e12, "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle", "seconds": secs,
+            "sample": f"fp64 oracle fwd+bwd, kv groups {ORACLE_SAMPLE['kv_groups']} ({2 * (w.Hq // w.Hkv)} query heads), "
+                      f"sequences {ORACLE_SAMPLE['seqs']} of {args.workload}"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default="dense",
+                    choices=("tiny", "dense", "window", "varlen", "long", "long_window"))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+/*
+ * sinkattn.h -- C ABI of libsinkattn.so: causal / sliding-window / varlen
+ * attention with one learnable sink logit per query head, forward and
+ * backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed. Page "GPT-OSS Agentic RL Training: A Practical
+ * Retrospective", section "The Role of Attention Sinks": each head has a
+ * learnable scalar S_h that acts as a virtual token inside the softmax; section
+ * "Implementation in FlashAttention v3": a forward with sinks, plus a backward
+ * that also returns dL/dS_h. The pages give no formula; this library takes the
+ * plain reading: exp(S_h) joins the softmax denominator and the virtual token
+ * has no value vector. For sequence b, query head h, local row i and every key
+ * j the mask allows:
+ *
+ *     s_ij  = scale * q_i . k_j            (k, v of kv head h / (Hq / Hkv))
+ *     LSE_i = log(exp(S_h) + sum_j exp(s_ij))        (natural log)
+ *     P_ij  = exp(s_ij - LSE_i),   O_i = sum_j P_ij v_j
+ *     dS_h  = - sum_{b,i} exp(S_h - LSE_i) * (dO_i . O_i)
+ *
+ * and dq, dk, dv are the gradients of the same function (dk, dv summed over
+ * the query heads that share a kv head).
+ *
+ * Mask. Key j is visible from row i (both local to their sequence) iff
+ * j <= i when causal, and additionally i - j < window when window > 0: a
+ * window of W keys is the W most recent keys, the diagonal included.
+ * Sequences never see each other.
+ *
+ * Data layout (all device memory, caller-owned):
+ *   q        bf16 [total, Hq,  64], token row stride q_row_stride elements
+ *   k, v     bf16 [total, Hkv, 64], token row strides k_row_stride, v_row_stride
+ *   o, dout, dq   bf16 [total, Hq, 64] contiguous
+ *   dk, dv        bf16 [total, Hkv, 64] contiguous
+ *   lse      fp32 [Hq, total] (head-major)
+ *   sinks, dsinks  fp32 [Hq]
+ *   cu_seqlens int32 [nseq + 1]: cu[0] = 0, non-decreasing, cu[nseq] = total.
+ * Within a token row the heads are contiguous (head stride 64) and the 64
+ * features are contiguous. Row strides must be multiples of 8 elements and
+ * every tensor pointer must be 16-byte aligned.
+ *
+ * Ownership and threading. The library never allocates or frees device
+ * memory: the caller passes a workspace of at least the size the matching
+ * *_workspace_size() call returns. All work is enqueued on the given stream
+ * (a cudaStream_t passed as void*; NULL = legacy default stream) and the call
+ * returns without synchronising. Two calls that share a workspace must not
+ * overlap on the GPU.
+ *
+ * Errors. Arguments are checked on the host before anything is launched;
+ * a bad argument returns SINKATTN_ERR_INVALID_ARG or SINKATTN_ERR_UNSUPPORTED
+ * and launches nothing. cu_seqlens lives on the device and is checked there:
+ * a malformed array makes every kernel skip its work and records
+ * SINKATTN_ERR_INVALID_ARG in the device error word. Every wait inside a
+ * kernel is bounded; a wait that runs out records SINKATTN_ERR_TIMEOUT in the
+ * same word and the kernel returns. sinkattn_device_error() reads the word.
+ * A failed launch returns SINKATTN_ERR_CUDA. On any error the outputs are
+ * undefined. sinkattn_last_error_message() gives detail for the calling
+ * host thread.
+ */
+#ifndef SINKATTN_H_
+#define SINKATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SINKATTN_API __attribute__((visibility("default")))
+#else
+#define SINKATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sinkattn_status {
+  SINKATTN_OK = 0,
+  SINKATTN_ERR_INVALID_ARG = 1,
+  SINKATTN_ERR_UNSUPPORTED = 2,
+  SINKATTN_ERR_CUDA = 3,
+  SINKATTN_ERR_WORKSPACE = 4,
+  SINKATTN_ERR_TIMEOUT = 5
+} sinkattn_status;
+
+/* Forward: O and LSE (section "Implementation in FlashAttention v3", step 1). */
+typedef struct sinkattn_fwd_params {
+  const void* q;               /* bf16, see layout above                      */
+  const void* k;
+  const void* v;
+  const float* sinks;          /* fp32 [Hq]; NULL = no sink (S_h = -inf)      */
+  const int32_t* cu_seqlens;   /* device int32 [nseq + 1]                     */
+  void* o;                     /* out: bf16 [total, Hq, 64]                   */
+  float* lse;                  /* out: fp32 [Hq, total]; may be NULL          */
+  void* workspace;             /* >= sinkattn_fwd_workspace_size() bytes       */
+  size_t workspace_bytes;
+  void* timing_events[2];      /* optional cudaEvent_t pair recorded on the
+                                  stream just before and just after the main
+                                  attention kernel; NULL entries = none      */
+  int64_t q_row_stride;        /* elements between tokens; 0 = Hq * 64        */
+  int64_t k_row_stride;        /* 0 = Hkv * 64                                */
+  int64_t v_row_stride;        /* 0 = Hkv * 64                                */
+  int32_t nseq;                /* >= 0                                        */
+  int32_t total;               /* tokens = cu_seqlens[nseq] >= 0              */
+  int32_t max_seqlen;          /* >= every sequence length (checked on device) */
+  int32_t Hq;                  /* query heads, a multiple of Hkv              */
+  int32_t Hkv;                 /* key/value heads                             */
+  int32_t head_dim;            /* must be 64 (else SINKATTN_ERR_UNSUPPORTED)  */
+  int32_t causal;              /* 1 = causal mask, 0 = none                   */
+  int32_t window;              /* <= 0: no window; W > 0 needs causal = 1     */
+  float softmax_scale;         /* <= 0 selects 1/sqrt(head_dim)               */
+} sinkattn_fwd_params;
+
+/* Backward: dq, dk, dv and dL/dS_h (same section, step 2). The forward fields
+ * must describe the same problem the forward ran on; o and lse are its
+ * outputs. */
+typedef struct sinkattn_bwd_params {
+  sinkattn_fwd_params fwd;     /* fwd.o, fwd.lse are inputs here (lse required);
+                                  fwd.workspace is ignored                    */
+  const void* dout;            /* bf16 [total, Hq, 64] contiguous: dL/dO       */
+  void* dq;                    /* out: bf16 [total, Hq, 64]                    */
+  void* dk;                    /* out: bf16 [total, Hkv, 64]                   */
+  void* dv;                    /* out: bf16 [total, Hkv, 64]                   */
+  float* dsinks;               /* out: fp32 [Hq], overwritten (not accumulated);
+                                  may be NULL; all zero when sinks is NULL    */
+  void* workspace;             /* >= sinkattn_bwd_workspace_size() bytes       */
+  size_t workspace_bytes;
+  void* timing_events[2];      /* optional, around the main backward kernel    */
+} sinkattn_bwd_params;
+
+/* Workspace sizes in bytes for a problem of this shape (0 on bad input). */
+SINKATTN_API size_t sinkattn_fwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
+                                   int32_t head_dim);
+SINKATTN_API size_t sinkattn_bwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
+                                   int32_t head_dim);
+
+/* Enqueue the forward / backward on `stream`. */
+SINKATTN_API sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* params, void* stream);
+SINKATTN_API sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* params, void* stream);
+
+/* Static description of a status code; never NULL. */
+SINKATTN_API const char* sinkattn_status_string(int32_t status);
+
+/* Detail of the last error returned to the calling host thread ("" if none). */
+SINKATTN_API const char* sinkattn_last_error_message(void);
+
+/* Synchronises the current device and returns its device error word
+ * (SINKATTN_OK if no kernel recorded an error); clears it when reset != 0.
+ * Returns SINKATTN_ERR_CUDA if the word cannot be read. */
+SINKATTN_API int32_t sinkattn_device_error(int32_t reset);
+
+/* Number of kernels this library has launched in this process. */
+SINKATTN_API uint64_t sinkattn_launch_count(void);
+
+/* sizeof(sinkattn_fwd_params) for which = 0, sizeof(sinkattn_bwd_params) for
+ * which = 1, else 0: lets a binding check its mirror of the structs. */
+SINKATTN_API size_t sinkattn_params_size(int32_t which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKATTN_H_ */

@@ -63,7 +63,8 @@ def _load():
             fn.restype = ctypes.c_int
             fn.argtypes = [_dp, _dp, _dp, _dp, _dp, _ip, ctypes.c_int32, ctypes.c_int32,
                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                           ctypes.c_double, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int32]
+                           ctypes.c_double, ctypes.c_int32, _dp, _dp, _dp, _dp, _dp, _dp,
+                           ctypes.c_int32]
             _lib = lib
     return _lib
 
@@ -77,7 +78,7 @@ def default_threads() -> int:
 
 
 def sinkattn(q, k, v, sinks, cu_seqlens, *, causal=True, window=0, scale=None,
-             dout=None, want=("o", "lse"), nthreads=None):
+             dout=None, want=("o", "lse"), nthreads=None, first_row=0):
     """Evaluate the definition on host arrays.
 
     q [total, Hq, d], k/v [total, Hkv, d], dout [total, Hq, d] (any float type,
@@ -85,6 +86,8 @@ def sinkattn(q, k, v, sinks, cu_seqlens, *, causal=True, window=0, scale=None,
     sinks [Hq] or None (no sink); cu_seqlens int [nseq+1].
     ``want`` picks outputs among o, lse, dq, dk, dv, dsinks. Returns a dict of
     fp64 arrays: o [total,Hq,d], lse [Hq,total], dq, dk, dv, dsinks [Hq].
+    ``first_row`` > 0 (causal only) computes only local rows and keys >=
+    first_row of each sequence; entries elsewhere stay zero.
     """
     lib = _load()
     q = np.ascontiguousarray(q, dtype=np.float64)
@@ -107,7 +110,7 @@ def sinkattn(q, k, v, sinks, cu_seqlens, *, causal=True, window=0, scale=None,
         out[name] = np.zeros(shapes[name], dtype=np.float64)
     rc = lib.oracle_sinkattn(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(g),
                              cu.ctypes.data_as(_ip), nseq, Hq, Hkv, d, int(bool(causal)),
-                             int(window), float(scale),
+                             int(window), float(scale), int(first_row),
                              _ptr(out.get("o")), _ptr(out.get("lse")), _ptr(out.get("dq")),
                              _ptr(out.get("dk")), _ptr(out.get("dv")), _ptr(out.get("dsinks")),
                              int(nthreads or default_threads()))

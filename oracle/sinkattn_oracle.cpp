@@ -52,6 +52,7 @@ struct Problem {
   const double* dout;   // may be null: forward only
   const int32_t* cu;
   int32_t nseq, Hq, Hkv, d, causal, window;
+  int32_t first_row;  // rows and keys below this local index are skipped
   double scale;
 };
 
@@ -115,7 +116,7 @@ std::vector<Unit> make_units(const Problem& p, int heads) {
   for (int32_t b = 0; b < p.nseq; ++b) {
     const int64_t L = p.cu[b + 1] - p.cu[b];
     for (int h = 0; h < heads; ++h)
-      for (int64_t r = 0; r < L; r += kChunk) units.push_back({b, h, r});
+      for (int64_t r = p.first_row; r < L; r += kChunk) units.push_back({b, h, r});
   }
   return units;
 }
@@ -132,22 +133,30 @@ extern "C" {
 // total = cu_seqlens[nseq]. Any output pointer may be null to skip it.
 // dq/dk/dv/dsinks need dout. When sinks is null the sink is absent and
 // dsinks, if requested, is all zero.
+//
+// first_row > 0 restricts the work to local rows >= first_row and keys >=
+// first_row of every sequence (outputs elsewhere are left untouched, and
+// dsinks sums only those rows). Under a causal mask the rows that see such a
+// key all lie in that range, so dk and dv there are still complete; the rows
+// themselves always see all their keys.
 int oracle_sinkattn(const double* q, const double* k, const double* v,
                     const double* sinks, const double* dout,
                     const int32_t* cu_seqlens, int32_t nseq, int32_t Hq,
                     int32_t Hkv, int32_t d, int32_t causal, int32_t window,
-                    double scale, double* o, double* lse, double* dq,
-                    double* dk, double* dv, double* dsinks, int32_t nthreads) {
+                    double scale, int32_t first_row, double* o, double* lse,
+                    double* dq, double* dk, double* dv, double* dsinks,
+                    int32_t nthreads) {
   if (!q || !k || !v || !cu_seqlens || nseq < 0 || Hq <= 0 || Hkv <= 0 ||
       d <= 0 || Hq % Hkv != 0)
     return 1;
   if (window > 0 && !causal) return 1;
+  if (first_row < 0 || (first_row > 0 && !causal)) return 1;
   if ((dq || dk || dv || dsinks) && !dout) return 1;
   for (int32_t b = 0; b < nseq; ++b)
     if (cu_seqlens[b + 1] < cu_seqlens[b]) return 1;
   if (cu_seqlens[0] != 0) return 1;
 
-  Problem p{q, k, v, sinks, dout, cu_seqlens, nseq, Hq, Hkv, d, causal, window, scale};
+  Problem p{q, k, v, sinks, dout, cu_seqlens, nseq, Hq, Hkv, d, causal, window, first_row, scale};
   const int G = Hq / Hkv;
   const int64_t total = cu_seqlens[nseq];
   const bool want_bwd = dq || dk || dv || dsinks;
@@ -214,9 +223,10 @@ int oracle_sinkattn(const double* q, const double* k, const double* v,
   });
 
   if (lse)
-    for (int h = 0; h < Hq; ++h)
-      for (int64_t t = 0; t < total; ++t)
-        lse[(size_t)h * total + t] = lse_all[(size_t)h * total + t];
+    for (int32_t b = 0; b < nseq; ++b)
+      for (int h = 0; h < Hq; ++h)
+        for (int64_t t = cu_seqlens[b] + first_row; t < cu_seqlens[b + 1]; ++t)
+          lse[(size_t)h * total + t] = lse_all[(size_t)h * total + t];
 
   if (dsinks) {
     for (int h = 0; h < Hq; ++h) dsinks[h] = 0.0;

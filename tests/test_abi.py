@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/sinkattn.h declares, its parameter structs match the binding, and
+bad arguments are rejected on the host before anything is launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_learnable_sinks_gb300 import _binding
+from attention_learnable_sinks_gb300._binding import BwdParams, FwdParams
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sinkattn.h")).read()
+    return re.findall(r"SINKATTN_API\s+[\w\s\*]+?\b(sinkattn_\w+)\s*\(", src)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _binding.lib()
+    names = declared_functions()
+    assert len(names) >= 9
+    bound = {n for n, _, _ in _binding.SYMBOLS}
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+        assert n in bound, f"{n} not bound in _binding.SYMBOLS"
+
+
+def test_param_struct_sizes_match():
+    lib = _binding.lib()
+    assert lib.sinkattn_params_size(0) == ctypes.sizeof(FwdParams)
+    assert lib.sinkattn_params_size(1) == ctypes.sizeof(BwdParams)
+    assert lib.sinkattn_params_size(2) == 0
+
+
+def test_workspace_sizes():
+    lib = _binding.lib()
+    f = lib.sinkattn_fwd_workspace_size(4, 8192, 64, 8, 64)
+    b = lib.sinkattn_bwd_workspace_size(4, 8192, 64, 8, 64)
+    assert 0 < f < b
+    assert b >= 8192 * 64 * 64 * 4  # fp32 dq accumulator
+    assert lib.sinkattn_fwd_workspace_size(4, 8192, 64, 8, 128) == 0
+    assert lib.sinkattn_bwd_workspace_size(4, 8192, 63, 8, 64) == 0
+    assert lib.sinkattn_bwd_workspace_size(-1, 8192, 64, 8, 64) == 0
+
+
+def test_status_strings():
+    lib = _binding.lib()
+    for code in range(6):
+        assert lib.sinkattn_status_string(code)
+    assert lib.sinkattn_status_string(99) == b"unknown status"
+
+
+def _params(**kw):
+    p = FwdParams()
+    fake = 0x10000  # never dereferenced: every case below fails or returns before a launch
+    p.q = p.k = p.v = p.o = p.lse = p.cu_seqlens = fake
+    p.nseq, p.total, p.max_seqlen = 1, 128, 128
+    p.Hq, p.Hkv, p.head_dim, p.causal, p.window = 4, 2, 64, 1, 0
+    buf = (ctypes.c_uint8 * 4096)()
+    p.workspace, p.workspace_bytes = ctypes.addressof(buf), 4096
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p, buf
+
+
+@pytest.mark.parametrize("change,status", [
+    ({"head_dim": 128}, 2),
+    ({"Hq": 5}, 1),
+    ({"Hkv": 0}, 1),
+    ({"causal": 0, "window": 16}, 2),
+    ({"causal": 2}, 1),
+    ({"cu_seqlens": None}, 1),
+    ({"q": None}, 1),
+    ({"q": 0x10008}, 1),          # not 16-byte aligned
+    ({"q_row_stride": 4 * 64 + 4}, 1),
+    ({"k_row_stride": 64}, 1),     # does not cover both kv heads
+    ({"max_seqlen": 0}, 1),
+    ({"softmax_scale": float("nan")}, 1),
+    ({"workspace_bytes": 8}, 4),
+    ({"workspace": None}, 4),
+])
+def test_forward_rejects_bad_arguments(change, status):
+    lib = _binding.lib()
+    n0 = lib.sinkattn_launch_count()
+    p, buf = _params(**change)
+    assert lib.sinkattn_fwd(ctypes.byref(p), None) == status
+    assert lib.sinkattn_last_error_message()
+    assert lib.sinkattn_launch_count() == n0
+
+
+def test_empty_forward_needs_no_device():
+    lib = _binding.lib()
+    p, buf = _params(total=0, max_seqlen=0)
+    assert lib.sinkattn_fwd(ctypes.byref(p), None) == 0
+    assert lib.sinkattn_last_error_message() == b""
+
+
+def test_backward_rejects_missing_outputs():
+    lib = _binding.lib()
+    b = BwdParams()
+    p, buf = _params()
+    b.fwd = p
+    big = (ctypes.c_uint8 * (1 << 22))()
+    b.workspace, b.workspace_bytes = ctypes.addressof(big), len(big)
+    b.dout = b.dq = b.dk = 0x10000
+    b.dv = None
+    assert lib.sinkattn_bwd(ctypes.byref(b), None) == 1
+    b.dv = 0x10000
+    b.fwd.lse = None
+    assert lib.sinkattn_bwd(ctypes.byref(b), None) == 1
+    assert lib.sinkattn_bwd(None, None) == 1

@@ -327,3 +327,26 @@ def test_rejects_bad_arguments():
         oracle.sinkattn(q, k, v, s, cu, causal=False, window=2)
     with pytest.raises(ValueError):
         oracle.sinkattn(q, k[:, :1].repeat(3, 1), v[:, :1].repeat(3, 1), s, cu)
+
+
+@pytest.mark.parametrize("window", [0, 5])
+def test_first_row_restriction_matches_full_run(window):
+    # Rows >= r and keys >= r of each sequence, computed alone, equal the same
+    # entries of the unrestricted run (causal: only rows >= r see keys >= r).
+    rng = np.random.default_rng(16)
+    q, k, v, do, s, cu = rand_case(rng, [40, 9, 23], 4, 2, 8)
+    full = oracle.sinkattn(q, k, v, s, cu, window=window, dout=do, want=ALL)
+    r = 11
+    part = oracle.sinkattn(q, k, v, s, cu, window=window, dout=do, want=ALL, first_row=r)
+    dsum = np.zeros(4)
+    for b in range(3):
+        a, e = cu[b], cu[b + 1]
+        sl = slice(a + r, e)
+        for name in ("o", "dq", "dk", "dv"):
+            np.testing.assert_array_equal(part[name][sl], full[name][sl])
+            assert not np.any(part[name][a:a + r])
+        np.testing.assert_array_equal(part["lse"][:, sl], full["lse"][:, sl])
+        p_sink = np.exp(s[:, None] - full["lse"][:, sl])            # [Hq, rows]
+        D = np.einsum("thd,thd->ht", do[sl], full["o"][sl])
+        dsum += -(p_sink * D).sum(1)
+    np.testing.assert_allclose(part["dsinks"], dsum, rtol=1e-12)
