@@ -87,7 +87,7 @@ Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
     l.D = off;
     off += align256(sizeof(float) * (size_t)Hq * total);
     l.part = off;
-    off += align256(sizeof(float) * (size_t)Hq * l.nchunks);
+    off += align256(sizeof(float) * (size_t)Hq * l.capacity);
     l.dq_acc = off;
     off += align256(sizeof(float) * (size_t)total * Hq * kHeadDim);
   }
@@ -241,6 +241,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.sink_part = reinterpret_cast<float*>(ws + l.part);
   bp.dq_acc = reinterpret_cast<float*>(ws + l.dq_acc);
   bp.nchunks = l.nchunks;
+  bp.part_stride = l.capacity;
   TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
               l.capacity};
   TileList kt{reinterpret_cast<int32_t*>(ws + l.k_meta), reinterpret_cast<int2*>(ws + l.k_items),
@@ -255,7 +256,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   if (e == cudaSuccess) e = launch_bwd_dkdv(bp, kt, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward main");
   record(a->timing_events[1], s);
-  e = launch_bwd_finish(bp, s);
+  e = launch_bwd_finish(bp, kt, s);
   if (e != cudaSuccess) return cuda_fail(e, "sink gradient reduction");
   return SINKATTN_OK;
 }

@@ -5,16 +5,20 @@
 //
 // With the sink carrying no value, D_i = rowsum(dO_i * O_i) equals
 // sum_j P_ij dP_ij, so dS_ij = P_ij (dP_ij - D_i) as in plain attention, and the
-// sink's own gradient is -p_sink_i * D_i summed over rows, where
-// p_sink_i = exp(S_h - LSE_i).
+// sink's own gradient is dS_h = -sum_i p_sink_i D_i, p_sink_i = exp(S_h - LSE_i).
+//
+// dS_h is a sum with heavy cancellation (its terms change sign with dO), so it
+// is not formed from D, whose O is rounded to bf16: the key-stationary kernel
+// accumulates p_sink_i * P_ij * dP_ij from its fp32 P and dP instead, per
+// (key tile, head), and a final pass adds those partials in a fixed order.
 //
 // Kernels, in launch order:
-//   preprocess  one pass over (token, head) rows: D, and per-chunk partial
-//               sums of -p_sink * D (fixed-order block reduction)
+//   preprocess  one pass over (token, head) rows: D = rowsum(dO * O)
 //   dq          row-stationary: recompute P, dP, dS per key; dq = scale dS K
 //   dkdv        key-stationary over the whole GQA group:
-//               dv = sum P^T dO, dk = scale sum dS^T Q
-//   finish      dS_h = fixed-order fp64 sum of the partials
+//               dv = sum P^T dO, dk = scale sum dS^T Q, and the per-head
+//               partials of sum p_sink P dP
+//   finish      dS_h = -(fixed-order fp64 sum of the partials)
 #include <algorithm>
 #include <cmath>
 
@@ -56,7 +60,6 @@ preprocess_kernel(BwdProblem bp) {
   const Problem& p = bp.f;
   const int h = blockIdx.y;
   const int t = blockIdx.x * kPrepThreads + threadIdx.x;
-  float contrib = 0.f;
   if (t < p.total) {
     const uint4* o4 = reinterpret_cast<const uint4*>(p.o + ((int64_t)t * p.Hq + h) * 64);
     const uint4* g4 = reinterpret_cast<const uint4*>(bp.dout + ((int64_t)t * p.Hq + h) * 64);
@@ -73,16 +76,6 @@ preprocess_kernel(BwdProblem bp) {
       }
     }
     bp.D[(int64_t)h * p.total + t] = D;
-    if (p.sinks) contrib = -expf(p.sinks[h] - p.lse[(int64_t)h * p.total + t]) * D;
-  }
-  __shared__ float ws[kPrepThreads / 32];
-  contrib = warp_sum(contrib);
-  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = contrib;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < kPrepThreads / 32; ++w) s += ws[w];
-    bp.sink_part[(int64_t)h * bp.nchunks + blockIdx.x] = s;
   }
 }
 
@@ -179,7 +172,7 @@ dq_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__ m
 
 // ---------------------------------------------------------------- dk, dv
 constexpr size_t kDkvSmemBytes =
-    (4 * kTile * 64 + 2 * kChunk * kPad + 2 * kWarps * 64 + 2 * kChunk) * sizeof(float);
+    (4 * kTile * 64 + 2 * kChunk * kPad + 2 * kWarps * 64 + 3 * kChunk) * sizeof(float);
 
 __global__ void __launch_bounds__(kThreads)
 dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__ meta) {
@@ -195,7 +188,9 @@ dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__
   float* Sb = Pb + kWarps * 64;
   float* lse2 = Sb + kWarps * 64;
   float* Ds = lse2 + kChunk;
+  float* Ps = Ds + kChunk;            // p_sink of the chunk's rows
   __shared__ int s_w;
+  __shared__ float red[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwork = meta[0] * p.Hkv;
   for (;;) {
@@ -221,6 +216,8 @@ dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__
     seeing_rows(p.causal, p.window, L, c0, c1, &rlo, &rhi);
     for (int hh = 0; hh < p.G; ++hh) {
       const int h = kvh * p.G + hh;
+      const float sink2 = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
+      float sacc = 0.f;  // this thread's share of sum p_sink P dP for head h
       for (int q0 = rlo & ~(kChunk - 1); q0 < rhi; q0 += kChunk) {
         __syncthreads();
         for (int e = tid; e < kChunk * 64; e += kThreads) {
@@ -237,6 +234,7 @@ dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__
           const bool in = q0 + r < L;
           lse2[r] = in ? p.lse[(int64_t)h * p.total + base + q0 + r] * kLog2e : 0.f;
           Ds[r] = in ? bp.D[(int64_t)h * p.total + base + q0 + r] : 0.f;
+          Ps[r] = in && p.sinks ? exp2f(sink2 - lse2[r]) : 0.f;
         }
         __syncthreads();
         for (int kk = warp; kk < nkeys; kk += kWarps) {
@@ -256,6 +254,7 @@ dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__
           Pb[warp * 64 + lane + 32] = P1;
           Sb[warp * 64 + lane] = P0 * (g0 - Ds[lane]);
           Sb[warp * 64 + lane + 32] = P1 * (g1 - Ds[lane + 32]);
+          sacc += Ps[lane] * (P0 * g0) + Ps[lane + 32] * (P1 * g1);
           __syncwarp();
           float v0 = dVs[kk * 64 + 2 * lane], v1 = dVs[kk * 64 + 2 * lane + 1];
           float k0 = dKs[kk * 64 + 2 * lane], k1 = dKs[kk * 64 + 2 * lane + 1];
@@ -273,6 +272,16 @@ dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__
           __syncwarp();
         }
       }
+      // fixed-order reduction of the head's partial over the CTA
+      sacc = warp_sum(sacc);
+      __syncthreads();
+      if (lane == 0) red[warp] = sacc;
+      __syncthreads();
+      if (tid == 0) {
+        float s = 0.f;
+        for (int i = 0; i < kWarps; ++i) s += red[i];
+        bp.sink_part[(int64_t)h * bp.part_stride + w / p.Hkv] = s;
+      }
     }
     __syncthreads();
     for (int e = tid; e < nkeys * 64; e += kThreads) {
@@ -285,13 +294,15 @@ dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__
 }
 
 // ---------------------------------------------------------------- finish
-__global__ void finish_kernel(BwdProblem bp) {
+__global__ void finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
   if (h >= bp.f.Hq || !bp.dsinks) return;
   double acc = 0.0;
-  if (bp.f.sinks)
-    for (int c = 0; c < bp.nchunks; ++c) acc += (double)bp.sink_part[(int64_t)h * bp.nchunks + c];
-  bp.dsinks[h] = (float)acc;
+  if (bp.f.sinks) {
+    const int n = kmeta[0];
+    for (int c = 0; c < n; ++c) acc += (double)bp.sink_part[(int64_t)h * bp.part_stride + c];
+  }
+  bp.dsinks[h] = (float)(-acc);
 }
 
 template <class K>
@@ -332,8 +343,8 @@ cudaError_t launch_bwd_dkdv(const BwdProblem& p, const TileList& ktiles, int num
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_finish(const BwdProblem& p, cudaStream_t s) {
-  finish_kernel<<<(p.f.Hq + 127) / 128, 128, 0, s>>>(p);
+cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, cudaStream_t s) {
+  finish_kernel<<<(p.f.Hq + 127) / 128, 128, 0, s>>>(p, ktiles.meta);
   note_launch();
   return cudaGetLastError();
 }

@@ -35,9 +35,11 @@ struct BwdProblem {
   __nv_bfloat16* dv;
   float* dsinks;
   float* D;                    // [Hq, total] workspace: rowsum(dO * O)
-  float* sink_part;            // [Hq, nchunks] workspace
+  float* sink_part;            // [Hq, part_stride] workspace: per key tile
+                               // sum of p_sink * P * dP
   float* dq_acc;               // [total, Hq, 64] fp32 workspace
   int32_t nchunks;             // token chunks of the preprocess pass
+  int32_t part_stride;         // key-tile capacity
 };
 
 // Tile work list in the workspace: meta[0] = number of items, meta[1] = the
@@ -79,7 +81,7 @@ cudaError_t launch_bwd_dq(const BwdProblem& p, const TileList& qtiles, int num_s
                           cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdProblem& p, const TileList& ktiles, int num_sms,
                             cudaStream_t s);
-cudaError_t launch_bwd_finish(const BwdProblem& p, cudaStream_t s);
+cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, cudaStream_t s);
 
 // Counts kernel launches (sinkattn_launch_count).
 void note_launch(int n = 1);
