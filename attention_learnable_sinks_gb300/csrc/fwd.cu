@@ -1,174 +1,372 @@
-// Forward of sink attention: O and LSE.
+// Forward of sink attention on tcgen05 tensor cores: O and LSE.
 //
-// Online softmax over key chunks, seeded with the sink: the running maximum
+// Online softmax over 128-key tiles, seeded with the sink: the running maximum
 // starts at S_h and the running sum at exp(S_h - S_h) = 1, so the virtual
 // token enters the denominator once and adds nothing to the output (page
 // "GPT-OSS Agentic RL Training: A Practical Retrospective", section "The Role
 // of Attention Sinks").
 //
-// Persistent CTAs take (query tile, head) work items from the device-built
-// tile list, longest first; consecutive items are the heads of one tile, so
-// the GQA group's K/V rows are reused from L2.
+// One CTA owns one 128-row query tile of one head at a time (persistent,
+// static round robin over the device-built tile list, longest first; the
+// heads of a tile are consecutive work units, so a GQA group's K/V tiles are
+// reused from L2). Two CTAs share an SM, which interleaves one CTA's softmax
+// with the other's matrix products.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q tile, then K/V tiles into a 2-stage ring
+//   warp 1      UMMA issuer: S = Q K^T (SS, K-major both) and O += P V (P from
+//               tensor memory, V MN-major); S(j+1) is issued as soon as the
+//               softmax has read S(j), so it overlaps softmax(j)
+//   warps 2-5   softmax: one thread per query row (its TMEM lane); rescales O
+//               only when the row maximum grows by more than 2^8; writes P as
+//               bf16 into tensor memory; final O / l and LSE
+// Tensor memory (256 columns): S [0,128) fp32, P [128,192) bf16 pairs,
+// O [192,256) fp32.
 #include <algorithm>
 #include <cmath>
 
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace sinkattn {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 64;  // keys per staged chunk
-constexpr int kPad = 65;    // padded smem row (floats) for per-lane dot products
+using namespace sm100;
+
+constexpr int kThreads = 192;
+constexpr int kStages = 2;
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB of bf16
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.0f;  // log2 units
 
-constexpr size_t kSmemFloats = kTile * 64      // Qs
-                               + kChunk * kPad  // Ks
-                               + kChunk * 64    // Vs
-                               + kTile * 64     // Os (accumulator)
-                               + kWarps * 64    // Ps
-                               + 2 * kTile;     // m, l
-constexpr size_t kSmemBytes = kSmemFloats * sizeof(float);
+struct __align__(1024) Smem {
+  uint8_t q[kTileBytes];
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t q_full, q_empty, s_full, s_empty, p_full, o_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
+struct Unit {
+  int base, L, r0, nrows, h, kvh, kt0, kt1;
+};
+
+__device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int w) {
+  const int2 it = items[w / p.Hq];
+  Unit u;
+  u.h = w % p.Hq;
+  u.kvh = u.h / p.G;
+  u.base = p.cu[it.x];
+  u.L = p.cu[it.x + 1] - u.base;
+  u.r0 = it.y * kTile;
+  const int r1 = min(u.L, u.r0 + kTile);
+  u.nrows = r1 - u.r0;
+  int lo, hi;
+  visible_keys(p.causal, p.window, u.L, u.r0, r1, &lo, &hi);
+  u.kt0 = lo / kTile;
+  u.kt1 = (hi + kTile - 1) / kTile;
+  return u;
 }
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+
+// Wait that ignores the abort flag (still time-bounded): used only to drain
+// copies / products this thread issued before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) break;
 }
 
-__device__ __forceinline__ bool visible(const Problem& p, int i, int j, int L) {
-  if (j >= L) return false;
-  if (p.causal && j > i) return false;
-  if (p.window > 0 && i - j >= p.window) return false;
-  return true;
-}
+__global__ void __launch_bounds__(kThreads, 2)
+fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, Problem p, const int2* __restrict__ items,
+           const int32_t* __restrict__ meta) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const Guard g{&sm.abort, p.err};
 
-__global__ void __launch_bounds__(kThreads)
-fwd_kernel(Problem p, const int2* __restrict__ items, int32_t* __restrict__ meta) {
-  extern __shared__ float sm[];
-  float* Qs = sm;
-  float* Ks = Qs + kTile * 64;
-  float* Vs = Ks + kChunk * kPad;
-  float* Os = Vs + kChunk * 64;
-  float* Ps = Os + kTile * 64;
-  float* ms = Ps + kWarps * 64;
-  float* ls = ms + kTile;
-  __shared__ int s_w;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_empty, 128);
+    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tm_q);
+    tma_prefetch(&tm_k);
+    tma_prefetch(&tm_v);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
   const int nwork = meta[0] * p.Hq;
 
-  for (;;) {
-    __syncthreads();
-    if (tid == 0) s_w = atomicAdd(&meta[1], 1);
-    __syncthreads();
-    const int w = s_w;
-    if (w >= nwork) break;
-    const int2 it = items[w / p.Hq];
-    const int h = w % p.Hq, kvh = h / p.G;
-    const int base = p.cu[it.x], L = p.cu[it.x + 1] - base;
-    const int r0 = it.y * kTile, r1 = min(L, r0 + kTile), nrows = r1 - r0;
-    const float sink2 = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t nq = 0, nkv = 0;
+      for (int w = blockIdx.x; w < nwork; w += gridDim.x) {
+        const Unit u = decode(p, items, w);
+        if (!mbar_wait(&sm.q_empty, (nq & 1) ^ 1, g)) break;
+        mbar_expect_tx(&sm.q_full, kTileBytes);
+        tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base + u.r0);
+        ++nq;
+        bool ok = true;
+        for (int kt = u.kt0; kt < u.kt1; ++kt, ++nkv) {
+          const int s = nkv % kStages;
+          if (!mbar_wait(&sm.kv_empty[s], ((nkv / kStages) & 1) ^ 1, g)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.kv_full[s], 2 * kTileBytes);
+          tma_load_3d(sm.k[s], &tm_k, &sm.kv_full[s], 0, u.kvh, u.base + kt * kTile);
+          tma_load_3d(sm.v[s], &tm_v, &sm.kv_full[s], 0, u.kvh, u.base + kt * kTile);
+        }
+        if (!ok) break;
+      }
+      if (g.aborted()) {  // let issued copies land before the CTA exits
+        if (nq) drain_wait(&sm.q_full, (nq - 1) & 1);
+        for (uint32_t c = nkv > kStages ? nkv - kStages : 0; c < nkv; ++c)
+          drain_wait(&sm.kv_full[c % kStages], (c / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16(kTile, kTile, false, false);
+      const uint32_t idO = idesc_bf16(kTile, kHeadDim, false, true);
+      const uint32_t qa = smem_u32(sm.q);
+      uint32_t nq = 0, nkv = 0, ns = 0, np = 0;
+      auto issue_s = [&](int s) {
+        const uint32_t ka = smem_u32(sm.k[s]);
+#pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          umma_ss(tmem + kColS, sdesc_sw128(qa + 32 * k, 16, 1024),
+                  sdesc_sw128(ka + 32 * k, 16, 1024), idS, k > 0);
+      };
+      auto issue_pv = [&](int s, bool acc) {
+        const uint32_t va = smem_u32(sm.v[s]);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc_sw128(va + 2048 * k, 8192, 1024),
+                  idO, acc || k > 0);
+      };
+      bool ok = true;
+      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+        const Unit u = decode(p, items, w);
+        const int n = u.kt1 - u.kt0;
+        if (!mbar_wait(&sm.q_full, nq & 1, g)) break;
+        ++nq;
+        // S(0)
+        const uint32_t first = nkv;
+        if (!mbar_wait(&sm.kv_full[first % kStages], (first / kStages) & 1, g)) break;
+        if (!mbar_wait(&sm.s_empty, (ns & 1) ^ 1, g)) break;
+        ++ns;
+        tc_fence_after();
+        issue_s(first % kStages);
+        umma_commit(&sm.s_full);
+        if (n == 1) umma_commit(&sm.q_empty);
+        for (int jj = 0; jj < n; ++jj) {
+          const uint32_t cur = first + jj;
+          if (jj + 1 < n) {
+            const uint32_t nxt = cur + 1;
+            if (!mbar_wait(&sm.kv_full[nxt % kStages], (nxt / kStages) & 1, g) ||
+                !mbar_wait(&sm.s_empty, (ns & 1) ^ 1, g)) {
+              ok = false;
+              break;
+            }
+            ++ns;
+            tc_fence_after();
+            issue_s(nxt % kStages);
+            umma_commit(&sm.s_full);
+            if (jj + 2 == n) umma_commit(&sm.q_empty);
+          }
+          if (!mbar_wait(&sm.p_full, np & 1, g)) {
+            ok = false;
+            break;
+          }
+          ++np;
+          tc_fence_after();
+          issue_pv(cur % kStages, jj > 0);
+          umma_commit(&sm.kv_empty[cur % kStages]);
+          umma_commit(&sm.o_done);
+        }
+        nkv = first + n;
+      }
+      umma_commit(&sm.drain);  // every product issued above has completed
+      drain_wait(&sm.drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS, tP = tmem + lane_off + kColP,
+                   tO = tmem + lane_off + kColO;
+    const float sl2 = p.scale_log2;
+    uint32_t nsf = 0, nod = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+      const Unit u = decode(p, items, w);
+      const int n = u.kt1 - u.kt0;
+      const int i = u.r0 + r;
+      const int khi = p.causal ? min(i + 1, u.L) : u.L;
+      const int klo = p.window > 0 ? max(0, i - p.window + 1) : 0;
+      float m = p.sinks ? p.sinks[u.h] * kLog2e : -INFINITY;
+      float l = p.sinks ? 1.f : 0.f;
+      for (int jj = 0; jj < n; ++jj) {
+        const int c0 = (u.kt0 + jj) * kTile;
+        if (!mbar_wait(&sm.s_full, nsf & 1, g)) {
+          ok = false;
+          break;
+        }
+        ++nsf;
+        tc_fence_after();
+        float s[kTile];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + 32 * c, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(v[e]);
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.s_empty);
+        if (c0 < klo || c0 + kTile > khi) {
+          const int cl = klo - c0, ch = khi - c0;
+#pragma unroll
+          for (int c = 0; c < kTile; ++c)
+            if (c < cl || c >= ch) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < kTile; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+        // lazy rescale: keep the stale maximum unless it grew by > 2^8
+        const bool resc = m_new > m + kRescale;
+        const float alpha = resc ? ex2(m - m_new) : 1.f;
+        if (resc) {
+          l *= alpha;
+          m = m_new;
+        }
+        const float msub = m == -INFINITY ? 0.f : m;
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pa[32], pb[32];
+#pragma unroll
+        for (int c = 0; c < kTile / 2; ++c) {
+          const float p0 = ex2(fmaf(s[2 * c], sl2, -msub));
+          const float p1 = ex2(fmaf(s[2 * c + 1], sl2, -msub));
+          sum0 += p0;
+          sum1 += p1;
+          if (c < 32)
+            pa[c] = pack_bf16(p0, p1);
+          else
+            pb[c - 32] = pack_bf16(p0, p1);
+        }
+        l += sum0 + sum1;
+        if (jj > 0) {
+          // PV(jj-1) must be complete: it reads P and accumulates into O
+          if (!mbar_wait(&sm.o_done, nod & 1, g)) {
+            ok = false;
+            break;
+          }
+          ++nod;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, resc)) {  // O holds this unit's partial sum
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tO + 32 * c, v);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              tmem_st32(tO + 32 * c, v);
+            }
+          }
+        }
+        tmem_st32(tP, pa);
+        tmem_st32(tP + 32, pb);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full);
+      }
+      if (!ok) break;
+      // epilogue: O / l, LSE
+      if (!mbar_wait(&sm.o_done, nod & 1, g)) break;
+      ++nod;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint32_t ob[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + 32 * c, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          ob[16 * c + e] = pack_bf16(__uint_as_float(v[2 * e]) * inv,
+                                     __uint_as_float(v[2 * e + 1]) * inv);
+      }
+      if (r < u.nrows) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.o + ((int64_t)(u.base + u.r0 + r) * p.Hq + u.h) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+        if (p.lse)
+          p.lse[(int64_t)u.h * p.total + u.base + u.r0 + r] =
+              l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
 
-    for (int e = tid; e < kTile * 64; e += kThreads) {
-      const int r = e >> 6, d = e & 63;
-      float x = 0.f;
-      if (r < nrows)
-        x = __bfloat162float(p.q[(int64_t)(base + r0 + r) * p.q_stride + h * 64 + d]) * p.scale_log2;
-      Qs[e] = x;
-      Os[e] = 0.f;
-    }
-    for (int r = tid; r < kTile; r += kThreads) {
-      ms[r] = sink2;
-      ls[r] = p.sinks ? 1.f : 0.f;
-    }
-    int klo, khi;
-    visible_keys(p.causal, p.window, L, r0, r1, &klo, &khi);
-    for (int c0 = klo & ~(kChunk - 1); c0 < khi; c0 += kChunk) {
-      __syncthreads();
-      for (int e = tid; e < kChunk * 64; e += kThreads) {
-        const int j = e >> 6, d = e & 63;
-        float kx = 0.f, vx = 0.f;
-        if (c0 + j < L) {
-          kx = __bfloat162float(p.k[(int64_t)(base + c0 + j) * p.k_stride + kvh * 64 + d]);
-          vx = __bfloat162float(p.v[(int64_t)(base + c0 + j) * p.v_stride + kvh * 64 + d]);
-        }
-        Ks[j * kPad + d] = kx;
-        Vs[j * 64 + d] = vx;
-      }
-      __syncthreads();
-      for (int rr = warp; rr < nrows; rr += kWarps) {
-        const int i = r0 + rr;
-        const float* qrow = Qs + rr * 64;
-        float s0 = 0.f, s1 = 0.f;
-        for (int d = 0; d < 64; ++d) {
-          const float qd = qrow[d];
-          s0 += qd * Ks[lane * kPad + d];
-          s1 += qd * Ks[(lane + 32) * kPad + d];
-        }
-        if (!visible(p, i, c0 + lane, L)) s0 = -INFINITY;
-        if (!visible(p, i, c0 + lane + 32, L)) s1 = -INFINITY;
-        const float m_old = ms[rr];
-        const float m_new = fmaxf(m_old, warp_max(fmaxf(s0, s1)));
-        float alpha = 1.f, p0 = 0.f, p1 = 0.f;
-        if (m_new != -INFINITY) {
-          alpha = exp2f(m_old - m_new);
-          p0 = exp2f(s0 - m_new);
-          p1 = exp2f(s1 - m_new);
-        }
-        const float rs = warp_sum(p0 + p1);
-        Ps[warp * 64 + lane] = p0;
-        Ps[warp * 64 + lane + 32] = p1;
-        __syncwarp();
-        float a0 = Os[rr * 64 + 2 * lane] * alpha, a1 = Os[rr * 64 + 2 * lane + 1] * alpha;
-        for (int kk = 0; kk < kChunk; ++kk) {
-          const float pk = Ps[warp * 64 + kk];
-          a0 += pk * Vs[kk * 64 + 2 * lane];
-          a1 += pk * Vs[kk * 64 + 2 * lane + 1];
-        }
-        Os[rr * 64 + 2 * lane] = a0;
-        Os[rr * 64 + 2 * lane + 1] = a1;
-        const float l_old = ls[rr];
-        __syncwarp();
-        if (lane == 0) {
-          ms[rr] = m_new;
-          ls[rr] = l_old * alpha + rs;
-        }
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < nrows * 64; e += kThreads) {
-      const int r = e >> 6, d = e & 63;
-      const float l = ls[r];
-      p.o[(int64_t)(base + r0 + r) * p.Hq * 64 + h * 64 + d] =
-          __float2bfloat16_rn(l > 0.f ? Os[e] / l : 0.f);
-    }
-    if (p.lse)
-      for (int r = tid; r < nrows; r += kThreads) {
-        const float l = ls[r];
-        p.lse[(int64_t)h * p.total + base + r0 + r] =
-            l > 0.f ? (ms[r] + log2f(l)) * kLn2 : -INFINITY;
-      }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const Problem& p, const TileList& qtiles, int num_sms, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  CUtensorMap mq, mk, mv;
+  cudaError_t e = make_tmap_bf16_rows(&mq, p.q, p.Hq, p.total, p.q_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mk, p.k, p.Hkv, p.total, p.k_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mv, p.v, p.Hkv, p.total, p.v_stride);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t work = (int64_t)qtiles.capacity * p.Hq;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * 2);
   if (grid <= 0) return cudaSuccess;
-  fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, qtiles.items, qtiles.meta);
+  fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p, qtiles.items, qtiles.meta);
   note_launch();
   return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libsinkattn.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstddef>
@@ -71,6 +72,11 @@ __host__ __device__ inline void seeing_rows(int causal, int window, int L, int c
   int h = window > 0 ? c1 - 1 + window : L;
   *hi = h < L ? h : L;
 }
+
+// TMA descriptor for a bf16 [total, heads, 64] token-major tensor (row stride
+// in elements): 3-D {64, heads, total}, 128-byte swizzle, box {64, 1, 128}.
+cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
+                                int64_t row_stride);
 
 // Launchers (each returns the cudaGetLastError() of its launch).
 cudaError_t launch_build_tile_list(const Problem& p, int by_keys, const TileList& list,
