@@ -64,7 +64,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Workspace layout. Forward: [meta | q-tile items]. Backward:
-// [meta | q-tile items | meta | k-tile items | D | sink partials | dq_acc].
+// [meta | k-tile items | D | sink partials | dq_acc].
 struct Layout {
   size_t q_meta, q_items, k_meta, k_items, D, part, dq_acc, bytes;
   int32_t capacity, nchunks;
@@ -75,11 +75,12 @@ Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
   l.capacity = tile_capacity(nseq, total);
   l.nchunks = (total + kTile - 1) / kTile;
   size_t off = 0;
-  l.q_meta = off;
-  off += 256;
-  l.q_items = off;
-  off += align256(sizeof(int2) * (size_t)l.capacity);
-  if (bwd) {
+  if (!bwd) {
+    l.q_meta = off;
+    off += 256;
+    l.q_items = off;
+    off += align256(sizeof(int2) * (size_t)l.capacity);
+  } else {
     l.k_meta = off;
     off += 256;
     l.k_items = off;
@@ -87,7 +88,7 @@ Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
     l.D = off;
     off += align256(sizeof(float) * (size_t)Hq * total);
     l.part = off;
-    off += align256(sizeof(float) * (size_t)Hq * l.capacity);
+    off += align256(sizeof(float) * 4 * (size_t)Hq * l.capacity);
     l.dq_acc = off;
     off += align256(sizeof(float) * (size_t)total * Hq * kHeadDim);
   }
@@ -143,7 +144,8 @@ sinkattn_status check_fwd(const sinkattn_fwd_params* a, Problem* p) {
   p->Hkv = a->Hkv;
   p->G = a->Hq / a->Hkv;
   p->causal = a->causal;
-  p->window = a->window > 0 ? a->window : 0;
+  // a window at least as long as every sequence restricts nothing
+  p->window = (a->window > 0 && a->window < a->max_seqlen) ? a->window : 0;
   p->scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
   p->scale_log2 = p->scale * 1.4426950408889634f;
   return SINKATTN_OK;
@@ -194,6 +196,19 @@ cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, i
                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int total) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)total};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 4, (cuuint64_t)heads * kHeadDim * 4};
+  const cuuint32_t box[3] = {32, 1, (cuuint32_t)kTile};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -278,22 +293,18 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.dq_acc = reinterpret_cast<float*>(ws + l.dq_acc);
   bp.nchunks = l.nchunks;
   bp.part_stride = l.capacity;
-  TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
-              l.capacity};
   TileList kt{reinterpret_cast<int32_t*>(ws + l.k_meta), reinterpret_cast<int2*>(ws + l.k_items),
               l.capacity};
-  cudaError_t e = launch_build_tile_list(bp.f, 0, qt, s);
-  if (e == cudaSuccess) e = launch_build_tile_list(bp.f, 1, kt, s);
-  if (e != cudaSuccess) return cuda_fail(e, "tile lists");
+  cudaError_t e = launch_build_tile_list(bp.f, 1, kt, s);
+  if (e != cudaSuccess) return cuda_fail(e, "key-tile list");
   e = launch_bwd_preprocess(bp, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess");
   record(a->timing_events[0], s);
-  e = launch_bwd_dq(bp, qt, sms, s);
-  if (e == cudaSuccess) e = launch_bwd_dkdv(bp, kt, sms, s);
+  e = launch_bwd_main(bp, kt, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward main");
   record(a->timing_events[1], s);
-  e = launch_bwd_finish(bp, kt, s);
-  if (e != cudaSuccess) return cuda_fail(e, "sink gradient reduction");
+  e = launch_bwd_finish(bp, kt, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dq conversion / sink gradient");
   return SINKATTN_OK;
 }
 

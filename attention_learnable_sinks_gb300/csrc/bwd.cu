@@ -8,343 +8,605 @@
 // sink's own gradient is dS_h = -sum_i p_sink_i D_i, p_sink_i = exp(S_h - LSE_i).
 //
 // dS_h is a sum with heavy cancellation (its terms change sign with dO), so it
-// is not formed from D, whose O is rounded to bf16: the key-stationary kernel
+// is not formed from D, whose O is rounded to bf16: the main kernel
 // accumulates p_sink_i * P_ij * dP_ij from its fp32 P and dP instead, per
-// (key tile, head), and a final pass adds those partials in a fixed order.
+// (key tile, head), and the last pass adds those partials in a fixed order.
 //
 // Kernels, in launch order:
-//   preprocess  one pass over (token, head) rows: D = rowsum(dO * O)
-//   dq          row-stationary: recompute P, dP, dS per key; dq = scale dS K
-//   dkdv        key-stationary over the whole GQA group:
-//               dv = sum P^T dO, dk = scale sum dS^T Q, and the per-head
-//               partials of sum p_sink P dP
-//   finish      dS_h = -(fixed-order fp64 sum of the partials)
+//   preprocess  one pass over (token, head) rows: D = rowsum(dO * O); clears
+//               the fp32 dq accumulator
+//   main        key-stationary, on tcgen05 tensor cores (below)
+//   finish      dq = bf16(dq accumulator); dS_h = -(fixed-order fp64 sum of
+//               the partials)
+//
+// Main kernel. One CTA per SM owns a 128-key tile of one kv head at a time
+// (persistent, static round robin over the device-built key-tile list,
+// longest first) and loops over the G query heads of the group x the
+// 128-row query tiles that see the key tile, each split in two 64-row halves:
+//   S^T  = K Q^T      [128 keys x 64 q]   SS, both K-major        -> TMEM
+//   dP^T = V dO^T     [128 keys x 64 q]   SS, both K-major        -> TMEM
+//   P^T  = exp2(S^T * scale * log2e - LSE * log2e),  dS^T = P^T (dP^T - D)
+//        (softmax warpgroup, one key row per thread; written as bf16 to
+//        128-byte-swizzled shared memory)
+//   dV  += P^T dO     A = P^T (K-major), B = dO (MN-major)         TMEM
+//   dK  += dS^T Q     A = dS^T (K-major), B = Q (MN-major)         TMEM
+//   dQ   = dS K       per 128-row tile: A = the same dS^T buffer read
+//        M-major, B = K (MN-major); read out by a second warpgroup, scaled
+//        and added to the fp32 accumulator with a TMA bulk reduce-add.
+// S^T / dP^T are double-buffered in tensor memory, so the products of the
+// next half overlap the softmax of the current one. dK and dV stay in tensor
+// memory across the whole GQA group (no atomics) and are written once.
+//
+// Warp roles (320 threads): warp 0 TMA producer (all lanes stage LSE / D /
+// p_sink), warp 1 UMMA issuer, warps 2-5 softmax + dK/dV epilogue, warps
+// 6-9 dQ read-out. Tensor memory (512 columns): S^T [0,128) as two 64-column
+// buffers, dP^T [128,256), dV [256,320), dK [320,384), dQ [384,448).
 #include <algorithm>
 #include <cmath>
 
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace sinkattn {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 64;
-constexpr int kPad = 65;
+using namespace sm100;
+
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kPrepThreads = 128;  // tokens per preprocess block
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-__device__ __forceinline__ bool visible(const Problem& p, int i, int j, int L) {
-  if (i >= L || j >= L) return false;
-  if (p.causal && j > i) return false;
-  if (p.window > 0 && i - j >= p.window) return false;
-  return true;
-}
-
-__device__ __forceinline__ int next_item(int32_t* meta, int* slot) {
-  __syncthreads();
-  if (threadIdx.x == 0) *slot = atomicAdd(&meta[1], 1);
-  __syncthreads();
-  return *slot;
-}
+constexpr int kPrepThreads = 256;
 
 // ---------------------------------------------------------------- preprocess
 __global__ void __launch_bounds__(kPrepThreads)
 preprocess_kernel(BwdProblem bp) {
   const Problem& p = bp.f;
-  const int h = blockIdx.y;
-  const int t = blockIdx.x * kPrepThreads + threadIdx.x;
-  if (t < p.total) {
-    const uint4* o4 = reinterpret_cast<const uint4*>(p.o + ((int64_t)t * p.Hq + h) * 64);
-    const uint4* g4 = reinterpret_cast<const uint4*>(bp.dout + ((int64_t)t * p.Hq + h) * 64);
-    float D = 0.f;
+  const int64_t row = (int64_t)blockIdx.x * kPrepThreads + threadIdx.x;  // token * Hq + head
+  if (row >= (int64_t)p.total * p.Hq) return;
+  const int64_t t = row / p.Hq;
+  const int h = (int)(row % p.Hq);
+  const uint4* o4 = reinterpret_cast<const uint4*>(p.o + row * kHeadDim);
+  const uint4* g4 = reinterpret_cast<const uint4*>(bp.dout + row * kHeadDim);
+  float D = 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 a = o4[c], b = g4[c];
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  for (int c = 0; c < 8; ++c) {
+    const uint4 a = o4[c], b = g4[c];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(b2[e]);
-        D += x.x * y.x + x.y * y.y;
-      }
-    }
-    bp.D[(int64_t)h * p.total + t] = D;
-  }
-}
-
-// ---------------------------------------------------------------- dq
-constexpr size_t kDqSmemBytes =
-    (3 * kTile * 64 + 2 * kChunk * kPad + kWarps * 64 + 2 * kTile) * sizeof(float);
-
-__global__ void __launch_bounds__(kThreads)
-dq_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__ meta) {
-  const Problem& p = bp.f;
-  extern __shared__ float sm[];
-  float* Qs = sm;                    // q * scale * log2e
-  float* dOs = Qs + kTile * 64;
-  float* Acc = dOs + kTile * 64;     // sum_j dS_ij k_j
-  float* Ks = Acc + kTile * 64;
-  float* Vs = Ks + kChunk * kPad;
-  float* Bs = Vs + kChunk * kPad;    // per-warp dS row
-  float* lse2 = Bs + kWarps * 64;
-  float* Ds = lse2 + kTile;
-  __shared__ int s_w;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwork = meta[0] * p.Hq;
-  for (;;) {
-    const int w = next_item(meta, &s_w);
-    if (w >= nwork) break;
-    const int2 it = items[w / p.Hq];
-    const int h = w % p.Hq, kvh = h / p.G;
-    const int base = p.cu[it.x], L = p.cu[it.x + 1] - base;
-    const int r0 = it.y * kTile, r1 = min(L, r0 + kTile), nrows = r1 - r0;
-    for (int e = tid; e < kTile * 64; e += kThreads) {
-      const int r = e >> 6, d = e & 63;
-      float x = 0.f, g = 0.f;
-      if (r < nrows) {
-        x = __bfloat162float(p.q[(int64_t)(base + r0 + r) * p.q_stride + h * 64 + d]) * p.scale_log2;
-        g = __bfloat162float(bp.dout[((int64_t)(base + r0 + r) * p.Hq + h) * 64 + d]);
-      }
-      Qs[e] = x;
-      dOs[e] = g;
-      Acc[e] = 0.f;
-    }
-    for (int r = tid; r < kTile; r += kThreads) {
-      const bool in = r < nrows;
-      lse2[r] = in ? p.lse[(int64_t)h * p.total + base + r0 + r] * kLog2e : 0.f;
-      Ds[r] = in ? bp.D[(int64_t)h * p.total + base + r0 + r] : 0.f;
-    }
-    int klo, khi;
-    visible_keys(p.causal, p.window, L, r0, r1, &klo, &khi);
-    for (int c0 = klo & ~(kChunk - 1); c0 < khi; c0 += kChunk) {
-      __syncthreads();
-      for (int e = tid; e < kChunk * 64; e += kThreads) {
-        const int j = e >> 6, d = e & 63;
-        float kx = 0.f, vx = 0.f;
-        if (c0 + j < L) {
-          kx = __bfloat162float(p.k[(int64_t)(base + c0 + j) * p.k_stride + kvh * 64 + d]);
-          vx = __bfloat162float(p.v[(int64_t)(base + c0 + j) * p.v_stride + kvh * 64 + d]);
-        }
-        Ks[j * kPad + d] = kx;
-        Vs[j * kPad + d] = vx;
-      }
-      __syncthreads();
-      for (int rr = warp; rr < nrows; rr += kWarps) {
-        const int i = r0 + rr;
-        float s0 = 0.f, s1 = 0.f, g0 = 0.f, g1 = 0.f;
-        for (int d = 0; d < 64; ++d) {
-          const float qd = Qs[rr * 64 + d], gd = dOs[rr * 64 + d];
-          s0 += qd * Ks[lane * kPad + d];
-          s1 += qd * Ks[(lane + 32) * kPad + d];
-          g0 += gd * Vs[lane * kPad + d];
-          g1 += gd * Vs[(lane + 32) * kPad + d];
-        }
-        const float P0 = visible(p, i, c0 + lane, L) ? exp2f(s0 - lse2[rr]) : 0.f;
-        const float P1 = visible(p, i, c0 + lane + 32, L) ? exp2f(s1 - lse2[rr]) : 0.f;
-        Bs[warp * 64 + lane] = P0 * (g0 - Ds[rr]);
-        Bs[warp * 64 + lane + 32] = P1 * (g1 - Ds[rr]);
-        __syncwarp();
-        float a0 = Acc[rr * 64 + 2 * lane], a1 = Acc[rr * 64 + 2 * lane + 1];
-        for (int kk = 0; kk < kChunk; ++kk) {
-          const float ds = Bs[warp * 64 + kk];
-          a0 += ds * Ks[kk * kPad + 2 * lane];
-          a1 += ds * Ks[kk * kPad + 2 * lane + 1];
-        }
-        Acc[rr * 64 + 2 * lane] = a0;
-        Acc[rr * 64 + 2 * lane + 1] = a1;
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < nrows * 64; e += kThreads) {
-      const int r = e >> 6, d = e & 63;
-      bp.dq[((int64_t)(base + r0 + r) * p.Hq + h) * 64 + d] = __float2bfloat16_rn(Acc[e] * p.scale);
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(b2[e]);
+      D += x.x * y.x + x.y * y.y;
     }
   }
+  bp.D[(int64_t)h * p.total + t] = D;
+  float4* acc = reinterpret_cast<float4*>(bp.dq_acc + row * kHeadDim);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// ---------------------------------------------------------------- dk, dv
-constexpr size_t kDkvSmemBytes =
-    (4 * kTile * 64 + 2 * kChunk * kPad + 2 * kWarps * 64 + 3 * kChunk) * sizeof(float);
+// ---------------------------------------------------------------- main
+constexpr int kThreads = 320;
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB
+constexpr uint32_t kHalfBytes = kTileBytes / 2;        // 64 rows
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
 
-__global__ void __launch_bounds__(kThreads)
-dkdv_kernel(BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__ meta) {
+struct __align__(1024) Smem {
+  uint8_t k[kTileBytes];
+  uint8_t v[kTileBytes];
+  uint8_t q[2][kTileBytes];
+  uint8_t dout[2][kTileBytes];
+  uint8_t pt[2 * kTileBytes];   // P^T: two [128 keys][64 q] blocks
+  uint8_t dst[2 * kTileBytes];  // dS^T: same layout
+  uint8_t dq[2 * kTileBytes];   // dQ staging: two [128 q][32] fp32 boxes
+  float lse2[2][kTile];         // LSE * log2e (+inf for rows outside the sequence)
+  float dd[2][kTile];           // D
+  float psink[2][kTile];        // p_sink
+  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], sdp_full[2], sdp_empty[2];
+  uint64_t pds_full[2], pds_empty, dq_full, dq_empty, dkv_full, dkv_empty, drain;
+  uint64_t stg_free, stg_full;  // dQ staging buffer hand-off
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct Unit {
+  int item, base, L, c0, nkeys, kvh, qt0, nq;
+};
+
+__device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int w) {
+  Unit u;
+  u.item = w / p.Hkv;
+  const int2 it = items[u.item];
+  u.kvh = w % p.Hkv;
+  u.base = p.cu[it.x];
+  u.L = p.cu[it.x + 1] - u.base;
+  u.c0 = it.y * kTile;
+  const int c1 = min(u.L, u.c0 + kTile);
+  u.nkeys = c1 - u.c0;
+  int lo, hi;
+  seeing_rows(p.causal, p.window, u.L, u.c0, c1, &lo, &hi);
+  u.qt0 = lo / kTile;
+  u.nq = (hi + kTile - 1) / kTile - u.qt0;
+  return u;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) break;
+}
+
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0,
+                                                  int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__global__ void __maxnreg__(200)  // 320 threads x 200 registers fit one SM
+bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+           const __grid_constant__ CUtensorMap tm_dq, BwdProblem bp,
+           const int2* __restrict__ items, const int32_t* __restrict__ meta) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
   const Problem& p = bp.f;
-  extern __shared__ float sm[];
-  float* Ks = sm;
-  float* Vs = Ks + kTile * 64;
-  float* dKs = Vs + kTile * 64;
-  float* dVs = dKs + kTile * 64;
-  float* Qs = dVs + kTile * 64;       // unscaled q rows of the chunk
-  float* dOs = Qs + kChunk * kPad;
-  float* Pb = dOs + kChunk * kPad;
-  float* Sb = Pb + kWarps * 64;
-  float* lse2 = Sb + kWarps * 64;
-  float* Ds = lse2 + kChunk;
-  float* Ps = Ds + kChunk;            // p_sink of the chunk's rows
-  __shared__ int s_w;
-  __shared__ float red[kWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const Guard g{&sm.abort, p.err};
+
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.sdp_full[s], 1);
+      mbar_init(&sm.sdp_empty[s], 128);
+      mbar_init(&sm.pds_full[s], 128);
+    }
+    mbar_init(&sm.pds_empty, 1);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_empty, 128);
+    mbar_init(&sm.dkv_full, 1);
+    mbar_init(&sm.dkv_empty, 128);
+    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.stg_free, 1);
+    mbar_init(&sm.stg_full, 128);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tm_q);
+    tma_prefetch(&tm_k);
+    tma_prefetch(&tm_v);
+    tma_prefetch(&tm_do);
+    tma_prefetch(&tm_dq);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
   const int nwork = meta[0] * p.Hkv;
-  for (;;) {
-    const int w = next_item(meta, &s_w);
-    if (w >= nwork) break;
-    const int2 it = items[w / p.Hkv];
-    const int kvh = w % p.Hkv;
-    const int base = p.cu[it.x], L = p.cu[it.x + 1] - base;
-    const int c0 = it.y * kTile, c1 = min(L, c0 + kTile), nkeys = c1 - c0;
-    for (int e = tid; e < kTile * 64; e += kThreads) {
-      const int j = e >> 6, d = e & 63;
-      float kx = 0.f, vx = 0.f;
-      if (j < nkeys) {
-        kx = __bfloat162float(p.k[(int64_t)(base + c0 + j) * p.k_stride + kvh * 64 + d]);
-        vx = __bfloat162float(p.v[(int64_t)(base + c0 + j) * p.v_stride + kvh * 64 + d]);
+  const int G = p.G;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t nunit = 0, ntile = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+      const Unit u = decode(p, items, w);
+      if (!mbar_wait(&sm.kv_empty, (nunit & 1) ^ 1, g)) break;
+      if (lane == 0) {
+        mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
+        tma_load_3d(sm.k, &tm_k, &sm.kv_full, 0, u.kvh, u.base + u.c0);
+        tma_load_3d(sm.v, &tm_v, &sm.kv_full, 0, u.kvh, u.base + u.c0);
       }
-      Ks[e] = kx;
-      Vs[e] = vx;
-      dKs[e] = 0.f;
-      dVs[e] = 0.f;
-    }
-    int rlo, rhi;
-    seeing_rows(p.causal, p.window, L, c0, c1, &rlo, &rhi);
-    for (int hh = 0; hh < p.G; ++hh) {
-      const int h = kvh * p.G + hh;
-      const float sink2 = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
-      float sacc = 0.f;  // this thread's share of sum p_sink P dP for head h
-      for (int q0 = rlo & ~(kChunk - 1); q0 < rhi; q0 += kChunk) {
-        __syncthreads();
-        for (int e = tid; e < kChunk * 64; e += kThreads) {
-          const int r = e >> 6, d = e & 63;
-          float x = 0.f, g = 0.f;
-          if (q0 + r < L) {
-            x = __bfloat162float(p.q[(int64_t)(base + q0 + r) * p.q_stride + h * 64 + d]);
-            g = __bfloat162float(bp.dout[((int64_t)(base + q0 + r) * p.Hq + h) * 64 + d]);
-          }
-          Qs[r * kPad + d] = x;
-          dOs[r * kPad + d] = g;
+      ++nunit;
+      for (int i = 0; i < G * u.nq; ++i, ++ntile) {
+        const int h = u.kvh * G + i / u.nq;
+        const int q0 = (u.qt0 + i % u.nq) * kTile;
+        const int st = ntile & 1;
+        if (!mbar_wait(&sm.q_empty[st], ((ntile >> 1) & 1) ^ 1, g)) {
+          ok = false;
+          break;
         }
-        for (int r = tid; r < kChunk; r += kThreads) {
-          const bool in = q0 + r < L;
-          lse2[r] = in ? p.lse[(int64_t)h * p.total + base + q0 + r] * kLog2e : 0.f;
-          Ds[r] = in ? bp.D[(int64_t)h * p.total + base + q0 + r] : 0.f;
-          Ps[r] = in && p.sinks ? exp2f(sink2 - lse2[r]) : 0.f;
+        const float sink2 = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = lane * 4 + e;
+          const int q = q0 + r;
+          float l2 = INFINITY, d = 0.f, ps = 0.f;
+          if (q < u.L) {
+            const int64_t off = (int64_t)h * p.total + u.base + q;
+            l2 = p.lse[off] * kLog2e;
+            d = bp.D[off];
+            ps = p.sinks ? ex2(sink2 - l2) : 0.f;
+          }
+          sm.lse2[st][r] = l2;
+          sm.dd[st][r] = d;
+          sm.psink[st][r] = ps;
         }
-        __syncthreads();
-        for (int kk = warp; kk < nkeys; kk += kWarps) {
-          const int j = c0 + kk;
-          float s0 = 0.f, s1 = 0.f, g0 = 0.f, g1 = 0.f;
-          for (int d = 0; d < 64; ++d) {
-            const float kd = Ks[kk * 64 + d], vd = Vs[kk * 64 + d];
-            s0 += Qs[lane * kPad + d] * kd;
-            s1 += Qs[(lane + 32) * kPad + d] * kd;
-            g0 += dOs[lane * kPad + d] * vd;
-            g1 += dOs[(lane + 32) * kPad + d] * vd;
-          }
-          const float P0 = visible(p, q0 + lane, j, L) ? exp2f(s0 * p.scale_log2 - lse2[lane]) : 0.f;
-          const float P1 =
-              visible(p, q0 + lane + 32, j, L) ? exp2f(s1 * p.scale_log2 - lse2[lane + 32]) : 0.f;
-          Pb[warp * 64 + lane] = P0;
-          Pb[warp * 64 + lane + 32] = P1;
-          Sb[warp * 64 + lane] = P0 * (g0 - Ds[lane]);
-          Sb[warp * 64 + lane + 32] = P1 * (g1 - Ds[lane + 32]);
-          sacc += Ps[lane] * (P0 * g0) + Ps[lane + 32] * (P1 * g1);
-          __syncwarp();
-          float v0 = dVs[kk * 64 + 2 * lane], v1 = dVs[kk * 64 + 2 * lane + 1];
-          float k0 = dKs[kk * 64 + 2 * lane], k1 = dKs[kk * 64 + 2 * lane + 1];
-          for (int r = 0; r < kChunk; ++r) {
-            const float pr = Pb[warp * 64 + r], sr = Sb[warp * 64 + r];
-            v0 += pr * dOs[r * kPad + 2 * lane];
-            v1 += pr * dOs[r * kPad + 2 * lane + 1];
-            k0 += sr * Qs[r * kPad + 2 * lane];
-            k1 += sr * Qs[r * kPad + 2 * lane + 1];
-          }
-          dVs[kk * 64 + 2 * lane] = v0;
-          dVs[kk * 64 + 2 * lane + 1] = v1;
-          dKs[kk * 64 + 2 * lane] = k0;
-          dKs[kk * 64 + 2 * lane + 1] = k1;
-          __syncwarp();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(&sm.q_full[st], 2 * kTileBytes);
+          tma_load_3d(sm.q[st], &tm_q, &sm.q_full[st], 0, h, u.base + q0);
+          tma_load_3d(sm.dout[st], &tm_do, &sm.q_full[st], 0, h, u.base + q0);
         }
       }
-      // fixed-order reduction of the head's partial over the CTA
-      sacc = warp_sum(sacc);
-      __syncthreads();
-      if (lane == 0) red[warp] = sacc;
-      __syncthreads();
-      if (tid == 0) {
-        float s = 0.f;
-        for (int i = 0; i < kWarps; ++i) s += red[i];
-        bp.sink_part[(int64_t)h * bp.part_stride + w / p.Hkv] = s;
+    }
+    if (lane == 0 && g.aborted()) {
+      if (nunit) drain_wait(&sm.kv_full, (nunit - 1) & 1);
+      for (uint32_t c = ntile > 2 ? ntile - 2 : 0; c < ntile; ++c)
+        drain_wait(&sm.q_full[c & 1], (c >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16(kTile, 64, false, false);
+      const uint32_t idKV = idesc_bf16(kTile, kHeadDim, false, true);
+      const uint32_t idQ = idesc_bf16(kTile, kHeadDim, true, true);
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      const uint32_t pa = smem_u32(sm.pt), da = smem_u32(sm.dst);
+      uint32_t nunit = 0, ntile = 0, nsdp[2] = {0, 0}, npds[2] = {0, 0}, ndq = 0;
+      bool ok = true;
+      // S^T and dP^T of one half (hf) of a query tile
+      auto issue_sdp = [&](uint32_t tile, int hf) -> bool {
+        const int st = tile & 1;
+        if (!mbar_wait(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) return false;
+        ++nsdp[hf];
+        if (hf == 0 && !mbar_wait(&sm.q_full[st], (tile >> 1) & 1, g)) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sm.q[st]) + hf * kHalfBytes;
+        const uint32_t oa = smem_u32(sm.dout[st]) + hf * kHalfBytes;
+#pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k) {
+          umma_ss(tmem + kColS + 64 * hf, sdesc_sw128(ka + 32 * k, 16, 1024),
+                  sdesc_sw128(qa + 32 * k, 16, 1024), idS, k > 0);
+          umma_ss(tmem + kColDP + 64 * hf, sdesc_sw128(va + 32 * k, 16, 1024),
+                  sdesc_sw128(oa + 32 * k, 16, 1024), idS, k > 0);
+        }
+        umma_commit(&sm.sdp_full[hf]);
+        return true;
+      };
+      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+        const Unit u = decode(p, items, w);
+        const int N = 2 * G * u.nq;
+        if (!mbar_wait(&sm.kv_full, nunit & 1, g)) break;
+        if (!mbar_wait(&sm.dkv_empty, (nunit & 1) ^ 1, g)) break;
+        ++nunit;
+        const uint32_t tile0 = ntile;
+        if (!issue_sdp(tile0, 0) || !issue_sdp(tile0, 1)) break;
+        for (int n = 0; n < N; ++n) {
+          const int hf = n & 1;
+          const uint32_t tile = tile0 + (n >> 1);
+          const int st = tile & 1;
+          if (!mbar_wait(&sm.pds_full[hf], npds[hf] & 1, g)) {
+            ok = false;
+            break;
+          }
+          ++npds[hf];
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm.q[st]) + hf * kHalfBytes;
+          const uint32_t oa = smem_u32(sm.dout[st]) + hf * kHalfBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
+            const uint32_t acc = (n > 0 || k > 0) ? 1u : 0u;
+            umma_ss(tmem + kColDV, sdesc_sw128(pa + hf * kTileBytes + 32 * k, 16, 1024),
+                    sdesc_sw128(oa + 2048 * k, 8192, 1024), idKV, acc);
+            umma_ss(tmem + kColDK, sdesc_sw128(da + hf * kTileBytes + 32 * k, 16, 1024),
+                    sdesc_sw128(qa + 2048 * k, 8192, 1024), idKV, acc);
+          }
+          if (hf == 1) {
+            if (!mbar_wait(&sm.dq_empty, (ndq & 1) ^ 1, g)) {
+              ok = false;
+              break;
+            }
+            ++ndq;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time
+              umma_ss(tmem + kColDQ, sdesc_sw128(da + 2048 * k, kTileBytes, 1024),
+                      sdesc_sw128(ka + 2048 * k, 8192, 1024), idQ, k > 0);
+            umma_commit(&sm.pds_empty);
+            umma_commit(&sm.dq_full);
+            umma_commit(&sm.q_empty[st]);
+          }
+          if (n + 2 < N && !issue_sdp(tile0 + ((n + 2) >> 1), hf)) {
+            ok = false;
+            break;
+          }
+        }
+        ntile = tile0 + N / 2;
+        if (!ok) break;
+        umma_commit(&sm.dkv_full);
+        umma_commit(&sm.kv_empty);
+      }
+      umma_commit(&sm.drain);
+      drain_wait(&sm.drain, 0);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t nunit = 0, ntile = 0, nsd[2] = {0, 0};
+    bool ok = true;
+    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+      const Unit u = decode(p, items, w);
+      const int j = u.c0 + r;  // local key index
+      const bool jvalid = r < u.nkeys;
+      float sacc = 0.f;
+      for (int i = 0; i < G * u.nq && ok; ++i, ++ntile) {
+        const int hh = i / u.nq;
+        const int q0 = (u.qt0 + i % u.nq) * kTile;
+        const int st = ntile & 1;
+        // the producer's LSE / D / p_sink rows of this tile (acquire)
+        if (!mbar_wait(&sm.q_full[st], (ntile >> 1) & 1, g)) {
+          ok = false;
+          break;
+        }
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(&sm.sdp_full[hf], nsd[hf] & 1, g)) {
+            ok = false;
+            break;
+          }
+          ++nsd[hf];
+          tc_fence_after();
+          uint32_t sv[64], pv[64];
+          {
+            uint32_t a[32];
+            tmem_ld32(tmem + lane_off + kColS + 64 * hf, a);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[e] = a[e];
+            tmem_ld32(tmem + lane_off + kColS + 64 * hf + 32, a);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[32 + e] = a[e];
+            tmem_ld32(tmem + lane_off + kColDP + 64 * hf, a);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pv[e] = a[e];
+            tmem_ld32(tmem + lane_off + kColDP + 64 * hf + 32, a);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pv[32 + e] = a[e];
+          }
+          tc_fence_before();
+          mbar_arrive(&sm.sdp_empty[hf]);
+          // visible q columns of this key row: q in [qlo, qhi) (local rows)
+          const int qb = q0 + hf * 64;
+          const int qlo = p.causal ? j : 0;
+          const int qhi = p.window > 0 ? j + p.window : 0x7fffffff;
+          const bool full = jvalid && qb >= qlo && qb + 63 < qhi;
+          const int cl = qlo - qb, ch = qhi - qb;
+          const float* l2 = &sm.lse2[st][hf * 64];
+          const float* dd = &sm.dd[st][hf * 64];
+          const float* ps = &sm.psink[st][hf * 64];
+          uint32_t pP[32], pS[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float P0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -l2[c]));
+            float P1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l2[c + 1]));
+            if (!full) {
+              if (!jvalid || c < cl || c >= ch) P0 = 0.f;
+              if (!jvalid || c + 1 < cl || c + 1 >= ch) P1 = 0.f;
+            }
+            const float t0 = P0 * __uint_as_float(pv[c]);
+            const float t1 = P1 * __uint_as_float(pv[c + 1]);
+            sacc = fmaf(ps[c], t0, sacc);
+            sacc = fmaf(ps[c + 1], t1, sacc);
+            pP[c / 2] = pack_bf16(P0, P1);
+            pS[c / 2] = pack_bf16(fmaf(-P0, dd[c], t0), fmaf(-P1, dd[c + 1], t1));
+          }
+          if (hf == 0) {  // previous tile's products that read P^T / dS^T are done
+            if (!mbar_wait(&sm.pds_empty, (ntile & 1) ^ 1, g)) {
+              ok = false;
+              break;
+            }
+          }
+          uint8_t* prow = sm.pt + hf * kTileBytes;
+          uint8_t* srow = sm.dst + hf * kTileBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(prow + sw128_offset(r, c)) =
+                make_uint4(pP[4 * c], pP[4 * c + 1], pP[4 * c + 2], pP[4 * c + 3]);
+            *reinterpret_cast<uint4*>(srow + sw128_offset(r, c)) =
+                make_uint4(pS[4 * c], pS[4 * c + 1], pS[4 * c + 2], pS[4 * c + 3]);
+          }
+          fence_async_smem();
+          mbar_arrive(&sm.pds_full[hf]);
+        }
+        if (!ok) break;
+        if (i % u.nq == u.nq - 1) {
+          // head hh done: this warp's share of its sink-gradient partial
+          float v = sacc;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0)
+            bp.sink_part[((int64_t)(u.kvh * G + hh) * bp.part_stride + u.item) * 4 + quarter] = v;
+          sacc = 0.f;
+        }
+      }
+      if (!ok) break;
+      // epilogue: dK, dV rows of this key tile
+      if (!mbar_wait(&sm.dkv_full, nunit & 1, g)) break;
+      ++nunit;
+      tc_fence_after();
+      uint32_t ov[32], ok32[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + kColDV + 32 * c, a);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          ov[16 * c + e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+        tmem_ld32(tmem + lane_off + kColDK + 32 * c, a);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          ok32[16 * c + e] = pack_bf16(__uint_as_float(a[2 * e]) * p.scale,
+                                       __uint_as_float(a[2 * e + 1]) * p.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.dkv_empty);
+      if (jvalid) {
+        const int64_t off = ((int64_t)(u.base + j) * p.Hkv + u.kvh) * kHeadDim;
+        uint4* dv = reinterpret_cast<uint4*>(bp.dv + off);
+        uint4* dk = reinterpret_cast<uint4*>(bp.dk + off);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          dv[c] = make_uint4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+          dk[c] = make_uint4(ok32[4 * c], ok32[4 * c + 1], ok32[4 * c + 2], ok32[4 * c + 3]);
+        }
       }
     }
-    __syncthreads();
-    for (int e = tid; e < nkeys * 64; e += kThreads) {
-      const int j = e >> 6, d = e & 63;
-      const int64_t off = ((int64_t)(base + c0 + j) * p.Hkv + kvh) * 64 + d;
-      bp.dk[off] = __float2bfloat16_rn(dKs[e] * p.scale);
-      bp.dv[off] = __float2bfloat16_rn(dVs[e]);
+  } else {
+    // ------------------------------------------------------------ dQ read-out
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool issuer = threadIdx.x == 192;
+    uint32_t ndq = 0, nstg = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+      const Unit u = decode(p, items, w);
+      for (int i = 0; i < G * u.nq; ++i) {
+        const int h = u.kvh * G + i / u.nq;
+        const int q0 = (u.qt0 + i % u.nq) * kTile;
+        if (!mbar_wait(&sm.dq_full, ndq & 1, g)) {
+          ok = false;
+          break;
+        }
+        ++ndq;
+        tc_fence_after();
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_off + kColDQ, a);
+        tmem_ld32(tmem + lane_off + kColDQ + 32, b);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        if (issuer) {
+          bulk_wait_read0();  // the previous reduce has read the staging buffer
+          mbar_arrive(&sm.stg_free);
+        }
+        if (!mbar_wait(&sm.stg_free, nstg & 1, g)) {
+          ok = false;
+          break;
+        }
+        uint8_t* box0 = sm.dq;
+        uint8_t* box1 = sm.dq + kTileBytes;
+        const float sc = p.scale;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<float4*>(box0 + sw128_offset(r, c)) =
+              make_float4(__uint_as_float(a[4 * c]) * sc, __uint_as_float(a[4 * c + 1]) * sc,
+                          __uint_as_float(a[4 * c + 2]) * sc, __uint_as_float(a[4 * c + 3]) * sc);
+          *reinterpret_cast<float4*>(box1 + sw128_offset(r, c)) =
+              make_float4(__uint_as_float(b[4 * c]) * sc, __uint_as_float(b[4 * c + 1]) * sc,
+                          __uint_as_float(b[4 * c + 2]) * sc, __uint_as_float(b[4 * c + 3]) * sc);
+        }
+        fence_async_smem();
+        mbar_arrive(&sm.stg_full);
+        if (issuer) {
+          if (!mbar_wait(&sm.stg_full, nstg & 1, g)) {
+            ok = false;
+            break;
+          }
+          tma_reduce_add_3d(&tm_dq, box0, 0, h, u.base + q0);
+          tma_reduce_add_3d(&tm_dq, box1, 32, h, u.base + q0);
+          bulk_commit();
+        }
+        ++nstg;
+      }
     }
+    if (issuer) bulk_wait0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // ---------------------------------------------------------------- finish
-__global__ void finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
-  const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  if (h >= bp.f.Hq || !bp.dsinks) return;
-  double acc = 0.0;
-  if (bp.f.sinks) {
-    const int n = kmeta[0];
-    for (int c = 0; c < n; ++c) acc += (double)bp.sink_part[(int64_t)h * bp.part_stride + c];
-  }
-  bp.dsinks[h] = (float)(-acc);
-}
+constexpr int kFinishThreads = 256;
 
-template <class K>
-cudaError_t allow_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+__global__ void __launch_bounds__(kFinishThreads)
+finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
+  const Problem& p = bp.f;
+  if (blockIdx.x == 0 && bp.dsinks) {
+    for (int h = threadIdx.x; h < p.Hq; h += kFinishThreads) {
+      double acc = 0.0;
+      if (p.sinks) {
+        const int n = kmeta[0];
+        const float* part = bp.sink_part + (int64_t)h * bp.part_stride * 4;
+        for (int c = 0; c < 4 * n; ++c) acc += (double)part[c];
+      }
+      bp.dsinks[h] = (float)(-acc);
+    }
+  }
+  const int64_t n8 = (int64_t)p.total * p.Hq * kHeadDim / 8;
+  for (int64_t e = (int64_t)blockIdx.x * kFinishThreads + threadIdx.x; e < n8;
+       e += (int64_t)gridDim.x * kFinishThreads) {
+    const float4 a = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e];
+    const float4 b = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e + 1];
+    reinterpret_cast<uint4*>(bp.dq)[e] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w),
+                                                    pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s) {
-  if (p.nchunks == 0) return cudaSuccess;
-  preprocess_kernel<<<dim3(p.nchunks, p.f.Hq), kPrepThreads, 0, s>>>(p);
+  const int64_t rows = (int64_t)p.f.total * p.f.Hq;
+  if (rows == 0) return cudaSuccess;
+  preprocess_kernel<<<(unsigned)((rows + kPrepThreads - 1) / kPrepThreads), kPrepThreads, 0, s>>>(
+      p);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq(const BwdProblem& p, const TileList& qtiles, int num_sms,
-                          cudaStream_t s) {
-  cudaError_t e = allow_smem(dq_kernel, kDqSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int64_t work = (int64_t)qtiles.capacity * p.f.Hq;
-  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms);
-  if (grid <= 0) return cudaSuccess;
-  dq_kernel<<<grid, kThreads, kDqSmemBytes, s>>>(p, qtiles.items, qtiles.meta);
-  note_launch();
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_dkdv(const BwdProblem& p, const TileList& ktiles, int num_sms,
+cudaError_t launch_bwd_main(const BwdProblem& p, const TileList& ktiles, int num_sms,
                             cudaStream_t s) {
-  cudaError_t e = allow_smem(dkdv_kernel, kDkvSmemBytes);
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  cudaError_t e = make_tmap_bf16_rows(&mq, p.f.q, p.f.Hq, p.f.total, p.f.q_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mk, p.f.k, p.f.Hkv, p.f.total, p.f.k_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mv, p.f.v, p.f.Hkv, p.f.total, p.f.v_stride);
+  if (e == cudaSuccess)
+    e = make_tmap_bf16_rows(&mdo, p.dout, p.f.Hq, p.f.total, (int64_t)p.f.Hq * kHeadDim);
+  if (e == cudaSuccess) e = make_tmap_f32_rows(&mdq, p.dq_acc, p.f.Hq, p.f.total);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t work = (int64_t)ktiles.capacity * p.f.Hkv;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms);
   if (grid <= 0) return cudaSuccess;
-  dkdv_kernel<<<grid, kThreads, kDkvSmemBytes, s>>>(p, ktiles.items, ktiles.meta);
+  bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mdo, mdq, p, ktiles.items,
+                                                ktiles.meta);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, cudaStream_t s) {
-  finish_kernel<<<(p.f.Hq + 127) / 128, 128, 0, s>>>(p, ktiles.meta);
+cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int num_sms,
+                              cudaStream_t s) {
+  const int64_t n8 = (int64_t)p.f.total * p.f.Hq * kHeadDim / 8;
+  const int64_t blocks = std::max<int64_t>(
+      1, std::min<int64_t>((n8 + kFinishThreads - 1) / kFinishThreads, (int64_t)num_sms * 8));
+  finish_kernel<<<(unsigned)blocks, kFinishThreads, 0, s>>>(p, ktiles.meta);
   note_launch();
   return cudaGetLastError();
 }

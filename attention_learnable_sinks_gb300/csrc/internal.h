@@ -36,8 +36,8 @@ struct BwdProblem {
   __nv_bfloat16* dv;
   float* dsinks;
   float* D;                    // [Hq, total] workspace: rowsum(dO * O)
-  float* sink_part;            // [Hq, part_stride] workspace: per key tile
-                               // sum of p_sink * P * dP
+  float* sink_part;            // [Hq, part_stride, 4] workspace: per key tile and
+                               // softmax warp, sum of p_sink * P * dP
   float* dq_acc;               // [total, Hq, 64] fp32 workspace
   int32_t nchunks;             // token chunks of the preprocess pass
   int32_t part_stride;         // key-tile capacity
@@ -78,16 +78,19 @@ __host__ __device__ inline void seeing_rows(int causal, int window, int L, int c
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
                                 int64_t row_stride);
 
+// TMA descriptor for the fp32 [total, heads, 64] dq accumulator (contiguous):
+// 3-D {64, heads, total}, 128-byte swizzle, box {32, 1, 128}.
+cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int total);
+
 // Launchers (each returns the cudaGetLastError() of its launch).
 cudaError_t launch_build_tile_list(const Problem& p, int by_keys, const TileList& list,
                                    cudaStream_t s);
 cudaError_t launch_fwd(const Problem& p, const TileList& qtiles, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s);
-cudaError_t launch_bwd_dq(const BwdProblem& p, const TileList& qtiles, int num_sms,
-                          cudaStream_t s);
-cudaError_t launch_bwd_dkdv(const BwdProblem& p, const TileList& ktiles, int num_sms,
+cudaError_t launch_bwd_main(const BwdProblem& p, const TileList& ktiles, int num_sms,
                             cudaStream_t s);
-cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, cudaStream_t s);
+cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int num_sms,
+                              cudaStream_t s);
 
 // Counts kernel launches (sinkattn_launch_count).
 void note_launch(int n = 1);
