@@ -88,7 +88,7 @@ Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
     l.D = off;
     off += align256(sizeof(float) * (size_t)Hq * total);
     l.part = off;
-    off += align256(sizeof(float) * 4 * (size_t)Hq * l.capacity);
+    off += align256(sizeof(float) * 8 * (size_t)Hq * l.capacity);
     l.dq_acc = off;
     off += align256(sizeof(float) * (size_t)total * Hq * kHeadDim);
   }

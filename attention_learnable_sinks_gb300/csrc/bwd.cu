@@ -33,14 +33,17 @@
 //   dQ   = dS K       per 128-row tile: A = the same dS^T buffer read
 //        M-major, B = K (MN-major); read out by a second warpgroup, scaled
 //        and added to the fp32 accumulator with a TMA bulk reduce-add.
-// S^T / dP^T are double-buffered in tensor memory, so the products of the
-// next half overlap the softmax of the current one. dK and dV stay in tensor
-// memory across the whole GQA group (no atomics) and are written once.
+// Each half has its own tensor-memory S^T / dP^T buffer and its own softmax
+// warpgroup, so the two halves of a tile run side by side and the products
+// of one half overlap the softmax of the other; dS^T is double-buffered by
+// tile so the dQ product stays off the softmax's path. dK and dV stay in
+// tensor memory across the whole GQA group (no atomics) and are written once.
 //
-// Warp roles (320 threads): warp 0 TMA producer (all lanes stage LSE / D /
-// p_sink), warp 1 UMMA issuer, warps 2-5 softmax + dK/dV epilogue, warps
-// 6-9 dQ read-out. Tensor memory (512 columns): S^T [0,128) as two 64-column
-// buffers, dP^T [128,256), dV [256,320), dK [320,384), dQ [384,448).
+// Warp roles (512 threads): warp 0 TMA producer (all lanes stage LSE / D /
+// p_sink), warp 1 UMMA issuer, warps 4-7 / 8-11 softmax of half 0 / 1 and
+// the dV / dK epilogue, warps 12-15 dQ read-out (warps 2-3 idle). Tensor
+// memory (512 columns): S^T [0,128) as two 64-column buffers, dP^T [128,256),
+// dV [256,320), dK [320,384), dQ [384,448).
 #include <algorithm>
 #include <cmath>
 
@@ -84,26 +87,26 @@ preprocess_kernel(BwdProblem bp) {
 }
 
 // ---------------------------------------------------------------- main
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;        // 64 rows
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr int kQStages = 2;
 
 struct __align__(1024) Smem {
   uint8_t k[kTileBytes];
   uint8_t v[kTileBytes];
-  uint8_t q[2][kTileBytes];
-  uint8_t dout[2][kTileBytes];
-  uint8_t pt[2 * kTileBytes];   // P^T: two [128 keys][64 q] blocks
-  uint8_t dst[2 * kTileBytes];  // dS^T: same layout
-  uint8_t dq[2 * kTileBytes];   // dQ staging: two [128 q][32] fp32 boxes
-  float lse2[2][kTile];         // LSE * log2e (+inf for rows outside the sequence)
-  float dd[2][kTile];           // D
-  float psink[2][kTile];        // p_sink
-  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], sdp_full[2], sdp_empty[2];
-  uint64_t pds_full[2], pds_empty, dq_full, dq_empty, dkv_full, dkv_empty, drain;
-  uint64_t stg_free, stg_full;  // dQ staging buffer hand-off
+  uint8_t q[kQStages][kTileBytes];
+  uint8_t dout[kQStages][kTileBytes];
+  uint8_t pt[2 * kTileBytes];      // P^T: two [128 keys][64 q] blocks (one per half)
+  uint8_t dst[2][2 * kTileBytes];  // dS^T, double-buffered by tile parity
+  uint8_t dq[kTileBytes];          // dQ staging: one [128 q][32] fp32 box
+  float4 rowinfo[kQStages][kTile];  // per query row: {LSE*log2e (+inf outside
+                                    // the sequence), D, p_sink, 0}
+  uint64_t kv_full, kv_empty, q_full[kQStages], q_empty[kQStages];
+  uint64_t sdp_full[2], sdp_empty[2], pds_full[2], p_free[2], ds_free[2];
+  uint64_t dq_full, dq_empty, dkv_full, dkv_empty, stg_free, stg_full, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -154,7 +157,7 @@ __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-__global__ void __maxnreg__(200)  // 320 threads x 200 registers fit one SM
+__global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
            const __grid_constant__ CUtensorMap tm_dq, BwdProblem bp,
@@ -170,21 +173,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     sm.abort = 0;
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQStages; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.sdp_full[s], 1);
       mbar_init(&sm.sdp_empty[s], 128);
       mbar_init(&sm.pds_full[s], 128);
+      mbar_init(&sm.p_free[s], 1);
+      mbar_init(&sm.ds_free[s], 1);
     }
-    mbar_init(&sm.pds_empty, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_empty, 128);
     mbar_init(&sm.dkv_full, 1);
-    mbar_init(&sm.dkv_empty, 128);
-    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.dkv_empty, 256);
     mbar_init(&sm.stg_free, 1);
     mbar_init(&sm.stg_full, 128);
+    mbar_init(&sm.drain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -220,26 +226,28 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int i = 0; i < G * u.nq; ++i, ++ntile) {
         const int h = u.kvh * G + i / u.nq;
         const int q0 = (u.qt0 + i % u.nq) * kTile;
-        const int st = ntile & 1;
-        if (!mbar_wait(&sm.q_empty[st], ((ntile >> 1) & 1) ^ 1, g)) {
+        const int st = ntile % kQStages;
+        // global loads first (all in flight together), then the stage wait
+        float lv[4], dv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int q = q0 + lane * 4 + e;
+          const int64_t off = (int64_t)h * p.total + u.base + q;
+          lv[e] = q < u.L ? __ldg(p.lse + off) : 0.f;
+          dv[e] = q < u.L ? __ldg(bp.D + off) : 0.f;
+        }
+        const float sink2 = p.sinks ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+        if (!mbar_wait(&sm.q_empty[st], ((ntile / kQStages) & 1) ^ 1, g)) {
           ok = false;
           break;
         }
-        const float sink2 = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int r = lane * 4 + e;
-          const int q = q0 + r;
-          float l2 = INFINITY, d = 0.f, ps = 0.f;
-          if (q < u.L) {
-            const int64_t off = (int64_t)h * p.total + u.base + q;
-            l2 = p.lse[off] * kLog2e;
-            d = bp.D[off];
-            ps = p.sinks ? ex2(sink2 - l2) : 0.f;
-          }
-          sm.lse2[st][r] = l2;
-          sm.dd[st][r] = d;
-          sm.psink[st][r] = ps;
+          const int q = q0 + lane * 4 + e;
+          const bool in = q < u.L;
+          const float l2 = in ? lv[e] * kLog2e : INFINITY;
+          sm.rowinfo[st][lane * 4 + e] =
+              make_float4(l2, in ? dv[e] : 0.f, in && p.sinks ? ex2(sink2 - l2) : 0.f, 0.f);
         }
         __syncwarp();
         if (lane == 0) {
@@ -251,8 +259,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
     if (lane == 0 && g.aborted()) {
       if (nunit) drain_wait(&sm.kv_full, (nunit - 1) & 1);
-      for (uint32_t c = ntile > 2 ? ntile - 2 : 0; c < ntile; ++c)
-        drain_wait(&sm.q_full[c & 1], (c >> 1) & 1);
+      for (uint32_t c = ntile > kQStages ? ntile - kQStages : 0; c < ntile; ++c)
+        drain_wait(&sm.q_full[c % kQStages], (c / kQStages) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
@@ -260,16 +268,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const uint32_t idS = idesc_bf16(kTile, 64, false, false);
       const uint32_t idKV = idesc_bf16(kTile, kHeadDim, false, true);
       const uint32_t idQ = idesc_bf16(kTile, kHeadDim, true, true);
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
-      const uint32_t pa = smem_u32(sm.pt), da = smem_u32(sm.dst);
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), pa = smem_u32(sm.pt);
       uint32_t nunit = 0, ntile = 0, nsdp[2] = {0, 0}, npds[2] = {0, 0}, ndq = 0;
       bool ok = true;
-      // S^T and dP^T of one half (hf) of a query tile
+      // S^T and dP^T of half hf of a query tile (its Q / dO stage must be full)
       auto issue_sdp = [&](uint32_t tile, int hf) -> bool {
-        const int st = tile & 1;
+        const int st = tile % kQStages;
         if (!mbar_wait(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) return false;
         ++nsdp[hf];
-        if (hf == 0 && !mbar_wait(&sm.q_full[st], (tile >> 1) & 1, g)) return false;
         tc_fence_after();
         const uint32_t qa = smem_u32(sm.q[st]) + hf * kHalfBytes;
         const uint32_t oa = smem_u32(sm.dout[st]) + hf * kHalfBytes;
@@ -285,53 +291,71 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       };
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
         const Unit u = decode(p, items, w);
-        const int N = 2 * G * u.nq;
+        const int nt = G * u.nq;
         if (!mbar_wait(&sm.kv_full, nunit & 1, g)) break;
         if (!mbar_wait(&sm.dkv_empty, (nunit & 1) ^ 1, g)) break;
         ++nunit;
         const uint32_t tile0 = ntile;
-        if (!issue_sdp(tile0, 0) || !issue_sdp(tile0, 1)) break;
-        for (int n = 0; n < N; ++n) {
-          const int hf = n & 1;
-          const uint32_t tile = tile0 + (n >> 1);
-          const int st = tile & 1;
-          if (!mbar_wait(&sm.pds_full[hf], npds[hf] & 1, g)) {
-            ok = false;
-            break;
-          }
-          ++npds[hf];
-          tc_fence_after();
-          const uint32_t qa = smem_u32(sm.q[st]) + hf * kHalfBytes;
-          const uint32_t oa = smem_u32(sm.dout[st]) + hf * kHalfBytes;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
-            const uint32_t acc = (n > 0 || k > 0) ? 1u : 0u;
-            umma_ss(tmem + kColDV, sdesc_sw128(pa + hf * kTileBytes + 32 * k, 16, 1024),
-                    sdesc_sw128(oa + 2048 * k, 8192, 1024), idKV, acc);
-            umma_ss(tmem + kColDK, sdesc_sw128(da + hf * kTileBytes + 32 * k, 16, 1024),
-                    sdesc_sw128(qa + 2048 * k, 8192, 1024), idKV, acc);
-          }
-          if (hf == 1) {
-            if (!mbar_wait(&sm.dq_empty, (ndq & 1) ^ 1, g)) {
+        if (!mbar_wait(&sm.q_full[tile0 % kQStages], (tile0 / kQStages) & 1, g) ||
+            !issue_sdp(tile0, 0) || !issue_sdp(tile0, 1))
+          break;
+        for (int i = 0; i < nt && ok; ++i) {
+          const uint32_t tile = tile0 + i;
+          const int st = tile % kQStages, db = tile & 1;
+          const bool more = i + 1 < nt;
+          bool next_ready = false;  // Q / dO of the next tile landed
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait(&sm.pds_full[hf], npds[hf] & 1, g)) {
               ok = false;
               break;
             }
-            ++ndq;
+            ++npds[hf];
             tc_fence_after();
+            const uint32_t qa = smem_u32(sm.q[st]) + hf * kHalfBytes;
+            const uint32_t oa = smem_u32(sm.dout[st]) + hf * kHalfBytes;
+            const uint32_t da = smem_u32(sm.dst[db]) + hf * kTileBytes;
 #pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time
-              umma_ss(tmem + kColDQ, sdesc_sw128(da + 2048 * k, kTileBytes, 1024),
-                      sdesc_sw128(ka + 2048 * k, 8192, 1024), idQ, k > 0);
-            umma_commit(&sm.pds_empty);
-            umma_commit(&sm.dq_full);
-            umma_commit(&sm.q_empty[st]);
+            for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
+              const uint32_t acc = (i > 0 || hf > 0 || k > 0) ? 1u : 0u;
+              umma_ss(tmem + kColDV, sdesc_sw128(pa + hf * kTileBytes + 32 * k, 16, 1024),
+                      sdesc_sw128(oa + 2048 * k, 8192, 1024), idKV, acc);
+              umma_ss(tmem + kColDK, sdesc_sw128(da + 32 * k, 16, 1024),
+                      sdesc_sw128(qa + 2048 * k, 8192, 1024), idKV, acc);
+            }
+            umma_commit(&sm.p_free[hf]);
+            // look ahead: S^T / dP^T of the same half of the next tile, unless
+            // its Q / dO have not landed yet (then after dQ, below)
+            if (more) {
+              if (hf == 0)
+                next_ready = mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
+                                           ((tile + 1) / kQStages) & 1);
+              if (next_ready && !issue_sdp(tile + 1, hf)) {
+                ok = false;
+                break;
+              }
+            }
           }
-          if (n + 2 < N && !issue_sdp(tile0 + ((n + 2) >> 1), hf)) {
-            ok = false;
-            break;
+          if (!ok) break;
+          if (!mbar_wait(&sm.dq_empty, (ndq & 1) ^ 1, g)) break;
+          ++ndq;
+          tc_fence_after();
+          const uint32_t dsa = smem_u32(sm.dst[db]);
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time
+            umma_ss(tmem + kColDQ, sdesc_sw128(dsa + 2048 * k, kTileBytes, 1024),
+                    sdesc_sw128(ka + 2048 * k, 8192, 1024), idQ, k > 0);
+          umma_commit(&sm.ds_free[db]);
+          umma_commit(&sm.dq_full);
+          umma_commit(&sm.q_empty[st]);
+          if (more && !next_ready) {
+            if (!mbar_wait(&sm.q_full[(tile + 1) % kQStages], ((tile + 1) / kQStages) & 1, g) ||
+                !issue_sdp(tile + 1, 0) || !issue_sdp(tile + 1, 1)) {
+              ok = false;
+              break;
+            }
           }
         }
-        ntile = tile0 + N / 2;
+        ntile = tile0 + nt;
         if (!ok) break;
         umma_commit(&sm.dkv_full);
         umma_commit(&sm.kv_empty);
@@ -339,145 +363,132 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       umma_commit(&sm.drain);
       drain_wait(&sm.drain, 0);
     }
-  } else if (warp < 6) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax
+    // warpgroup hf handles half hf (query rows 64 hf .. 64 hf + 63) of every tile
+    const int hf = (warp - 4) / 4;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS + 64 * hf;
+    const uint32_t tdP = tmem + lane_off + kColDP + 64 * hf;
     const float sl2 = p.scale_log2;
-    uint32_t nunit = 0, ntile = 0, nsd[2] = {0, 0};
+    uint32_t nunit = 0, ntile = 0, nsd = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
       const Unit u = decode(p, items, w);
       const int j = u.c0 + r;  // local key index
       const bool jvalid = r < u.nkeys;
-      float sacc = 0.f;
+      const int qlo = p.causal ? j : 0;
+      const int qhi = p.window > 0 ? j + p.window : 0x7fffffff;
+      float sa0 = 0.f, sa1 = 0.f, sa2 = 0.f, sa3 = 0.f;
       for (int i = 0; i < G * u.nq && ok; ++i, ++ntile) {
         const int hh = i / u.nq;
-        const int q0 = (u.qt0 + i % u.nq) * kTile;
-        const int st = ntile & 1;
+        const int qb = (u.qt0 + i % u.nq) * kTile + 64 * hf;
+        const int st = ntile % kQStages, db = ntile & 1;
         // the producer's LSE / D / p_sink rows of this tile (acquire)
-        if (!mbar_wait(&sm.q_full[st], (ntile >> 1) & 1, g)) {
+        if (!mbar_wait(&sm.q_full[st], (ntile / kQStages) & 1, g) ||
+            !mbar_wait(&sm.sdp_full[hf], nsd & 1, g)) {
           ok = false;
           break;
         }
-        for (int hf = 0; hf < 2; ++hf) {
-          if (!mbar_wait(&sm.sdp_full[hf], nsd[hf] & 1, g)) {
-            ok = false;
-            break;
+        ++nsd;
+        tc_fence_after();
+        const bool full = jvalid && qb >= qlo && qb + 63 < qhi;
+        const int cl = qlo - qb, ch = qhi - qb;
+        const float4* info = &sm.rowinfo[st][64 * hf];
+        uint8_t* prow = sm.pt + hf * kTileBytes;
+        uint8_t* srow = sm.dst[db] + hf * kTileBytes;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {  // 16 query columns at a time
+          uint32_t sv[16], pv[16];
+          tmem_ld16x2(tS + 16 * c, tdP + 16 * c, sv, pv);
+          if (c == 3) {
+            tc_fence_before();
+            mbar_arrive(&sm.sdp_empty[hf]);
           }
-          ++nsd[hf];
-          tc_fence_after();
-          uint32_t sv[64], pv[64];
-          {
-            uint32_t a[32];
-            tmem_ld32(tmem + lane_off + kColS + 64 * hf, a);
+          uint32_t pP[8], pS[8];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sv[e] = a[e];
-            tmem_ld32(tmem + lane_off + kColS + 64 * hf + 32, a);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) sv[32 + e] = a[e];
-            tmem_ld32(tmem + lane_off + kColDP + 64 * hf, a);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) pv[e] = a[e];
-            tmem_ld32(tmem + lane_off + kColDP + 64 * hf + 32, a);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) pv[32 + e] = a[e];
-          }
-          tc_fence_before();
-          mbar_arrive(&sm.sdp_empty[hf]);
-          // visible q columns of this key row: q in [qlo, qhi) (local rows)
-          const int qb = q0 + hf * 64;
-          const int qlo = p.causal ? j : 0;
-          const int qhi = p.window > 0 ? j + p.window : 0x7fffffff;
-          const bool full = jvalid && qb >= qlo && qb + 63 < qhi;
-          const int cl = qlo - qb, ch = qhi - qb;
-          const float* l2 = &sm.lse2[st][hf * 64];
-          const float* dd = &sm.dd[st][hf * 64];
-          const float* ps = &sm.psink[st][hf * 64];
-          uint32_t pP[32], pS[32];
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            float P0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, -l2[c]));
-            float P1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l2[c + 1]));
+          for (int e = 0; e < 16; e += 2) {
+            const int col = 16 * c + e;
+            const float4 i0 = info[col], i1 = info[col + 1];  // {LSE*log2e, D, p_sink, -}
+            float P0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -i0.x));
+            float P1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -i1.x));
             if (!full) {
-              if (!jvalid || c < cl || c >= ch) P0 = 0.f;
-              if (!jvalid || c + 1 < cl || c + 1 >= ch) P1 = 0.f;
+              if (!jvalid || col < cl || col >= ch) P0 = 0.f;
+              if (!jvalid || col + 1 < cl || col + 1 >= ch) P1 = 0.f;
             }
-            const float t0 = P0 * __uint_as_float(pv[c]);
-            const float t1 = P1 * __uint_as_float(pv[c + 1]);
-            sacc = fmaf(ps[c], t0, sacc);
-            sacc = fmaf(ps[c + 1], t1, sacc);
-            pP[c / 2] = pack_bf16(P0, P1);
-            pS[c / 2] = pack_bf16(fmaf(-P0, dd[c], t0), fmaf(-P1, dd[c + 1], t1));
+            const float t0 = P0 * __uint_as_float(pv[e]);
+            const float t1 = P1 * __uint_as_float(pv[e + 1]);
+            if (e & 2) {
+              sa2 = fmaf(i0.z, t0, sa2);
+              sa3 = fmaf(i1.z, t1, sa3);
+            } else {
+              sa0 = fmaf(i0.z, t0, sa0);
+              sa1 = fmaf(i1.z, t1, sa1);
+            }
+            pP[e / 2] = pack_bf16(P0, P1);
+            pS[e / 2] = pack_bf16(fmaf(-P0, i0.y, t0), fmaf(-P1, i1.y, t1));
           }
-          if (hf == 0) {  // previous tile's products that read P^T / dS^T are done
-            if (!mbar_wait(&sm.pds_empty, (ntile & 1) ^ 1, g)) {
+          if (c == 0) {
+            // P^T half free (dV / dK of the previous tile done), and this
+            // tile's dS^T buffer free (dQ of the tile before that done)
+            if (!mbar_wait(&sm.p_free[hf], (ntile & 1) ^ 1, g) ||
+                !mbar_wait(&sm.ds_free[db], ((ntile >> 1) & 1) ^ 1, g)) {
               ok = false;
               break;
             }
           }
-          uint8_t* prow = sm.pt + hf * kTileBytes;
-          uint8_t* srow = sm.dst + hf * kTileBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4*>(prow + sw128_offset(r, c)) =
-                make_uint4(pP[4 * c], pP[4 * c + 1], pP[4 * c + 2], pP[4 * c + 3]);
-            *reinterpret_cast<uint4*>(srow + sw128_offset(r, c)) =
-                make_uint4(pS[4 * c], pS[4 * c + 1], pS[4 * c + 2], pS[4 * c + 3]);
+          for (int x = 0; x < 2; ++x) {
+            *reinterpret_cast<uint4*>(prow + sw128_offset(r, 2 * c + x)) =
+                make_uint4(pP[4 * x], pP[4 * x + 1], pP[4 * x + 2], pP[4 * x + 3]);
+            *reinterpret_cast<uint4*>(srow + sw128_offset(r, 2 * c + x)) =
+                make_uint4(pS[4 * x], pS[4 * x + 1], pS[4 * x + 2], pS[4 * x + 3]);
           }
-          fence_async_smem();
-          mbar_arrive(&sm.pds_full[hf]);
         }
         if (!ok) break;
+        fence_async_smem();
+        mbar_arrive(&sm.pds_full[hf]);
         if (i % u.nq == u.nq - 1) {
           // head hh done: this warp's share of its sink-gradient partial
-          float v = sacc;
+          float v = (sa0 + sa1) + (sa2 + sa3);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           if (lane == 0)
-            bp.sink_part[((int64_t)(u.kvh * G + hh) * bp.part_stride + u.item) * 4 + quarter] = v;
-          sacc = 0.f;
+            bp.sink_part[((int64_t)(u.kvh * G + hh) * bp.part_stride + u.item) * 8 + hf * 4 +
+                         quarter] = v;
+          sa0 = sa1 = sa2 = sa3 = 0.f;
         }
       }
       if (!ok) break;
-      // epilogue: dK, dV rows of this key tile
+      // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the dK rows
       if (!mbar_wait(&sm.dkv_full, nunit & 1, g)) break;
       ++nunit;
       tc_fence_after();
-      uint32_t ov[32], ok32[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + kColDV + 32 * c, a);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          ov[16 * c + e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-        tmem_ld32(tmem + lane_off + kColDK + 32 * c, a);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          ok32[16 * c + e] = pack_bf16(__uint_as_float(a[2 * e]) * p.scale,
-                                       __uint_as_float(a[2 * e + 1]) * p.scale);
-      }
+      uint32_t a[64];
+      tmem_ld64(tmem + lane_off + (hf == 0 ? kColDV : kColDK), a);
       tc_fence_before();
       mbar_arrive(&sm.dkv_empty);
       if (jvalid) {
-        const int64_t off = ((int64_t)(u.base + j) * p.Hkv + u.kvh) * kHeadDim;
-        uint4* dv = reinterpret_cast<uint4*>(bp.dv + off);
-        uint4* dk = reinterpret_cast<uint4*>(bp.dk + off);
+        const float sc = hf == 0 ? 1.f : p.scale;
+        uint32_t ob[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          dv[c] = make_uint4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
-          dk[c] = make_uint4(ok32[4 * c], ok32[4 * c + 1], ok32[4 * c + 2], ok32[4 * c + 3]);
-        }
+        for (int e = 0; e < 32; ++e)
+          ob[e] = pack_bf16(__uint_as_float(a[2 * e]) * sc, __uint_as_float(a[2 * e + 1]) * sc);
+        const int64_t off = ((int64_t)(u.base + j) * p.Hkv + u.kvh) * kHeadDim;
+        uint4* dst = reinterpret_cast<uint4*>((hf == 0 ? bp.dv : bp.dk) + off);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
       }
     }
-  } else {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ read-out
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool issuer = threadIdx.x == 192;
+    const bool issuer = threadIdx.x == 12 * 32;
     uint32_t ndq = 0, nstg = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
@@ -491,43 +502,39 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         ++ndq;
         tc_fence_after();
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + kColDQ, a);
-        tmem_ld32(tmem + lane_off + kColDQ + 32, b);
+        uint32_t a[64];
+        tmem_ld64(tmem + lane_off + kColDQ, a);
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
-        if (issuer) {
-          bulk_wait_read0();  // the previous reduce has read the staging buffer
-          mbar_arrive(&sm.stg_free);
-        }
-        if (!mbar_wait(&sm.stg_free, nstg & 1, g)) {
-          ok = false;
-          break;
-        }
-        uint8_t* box0 = sm.dq;
-        uint8_t* box1 = sm.dq + kTileBytes;
         const float sc = p.scale;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<float4*>(box0 + sw128_offset(r, c)) =
-              make_float4(__uint_as_float(a[4 * c]) * sc, __uint_as_float(a[4 * c + 1]) * sc,
-                          __uint_as_float(a[4 * c + 2]) * sc, __uint_as_float(a[4 * c + 3]) * sc);
-          *reinterpret_cast<float4*>(box1 + sw128_offset(r, c)) =
-              make_float4(__uint_as_float(b[4 * c]) * sc, __uint_as_float(b[4 * c + 1]) * sc,
-                          __uint_as_float(b[4 * c + 2]) * sc, __uint_as_float(b[4 * c + 3]) * sc);
-        }
-        fence_async_smem();
-        mbar_arrive(&sm.stg_full);
-        if (issuer) {
-          if (!mbar_wait(&sm.stg_full, nstg & 1, g)) {
+        for (int half = 0; half < 2 && ok; ++half, ++nstg) {
+          if (issuer) {
+            bulk_wait_read0();  // the previous reduce has read the staging buffer
+            mbar_arrive(&sm.stg_free);
+          }
+          if (!mbar_wait(&sm.stg_free, nstg & 1, g)) {
             ok = false;
             break;
           }
-          tma_reduce_add_3d(&tm_dq, box0, 0, h, u.base + q0);
-          tma_reduce_add_3d(&tm_dq, box1, 32, h, u.base + q0);
-          bulk_commit();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int e = 32 * half + 4 * c;
+            *reinterpret_cast<float4*>(sm.dq + sw128_offset(r, c)) =
+                make_float4(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc,
+                            __uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
+          }
+          fence_async_smem();
+          mbar_arrive(&sm.stg_full);
+          if (issuer) {
+            if (!mbar_wait(&sm.stg_full, nstg & 1, g)) {
+              ok = false;
+              break;
+            }
+            tma_reduce_add_3d(&tm_dq, sm.dq, 32 * half, h, u.base + q0);
+            bulk_commit();
+          }
         }
-        ++nstg;
+        if (!ok) break;
       }
     }
     if (issuer) bulk_wait0();
@@ -552,8 +559,8 @@ finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
       double acc = 0.0;
       if (p.sinks) {
         const int n = kmeta[0];
-        const float* part = bp.sink_part + (int64_t)h * bp.part_stride * 4;
-        for (int c = 0; c < 4 * n; ++c) acc += (double)part[c];
+        const float* part = bp.sink_part + (int64_t)h * bp.part_stride * 8;
+        for (int c = 0; c < 8 * n; ++c) acc += (double)part[c];
       }
       bp.dsinks[h] = (float)(-acc);
     }

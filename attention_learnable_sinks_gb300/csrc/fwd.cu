@@ -244,12 +244,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         ++nsf;
         tc_fence_after();
         float s[kTile];
+        {
+          uint32_t v[kTile];
+          tmem_ld128(tS, v);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + 32 * c, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(v[e]);
+          for (int e = 0; e < kTile; ++e) s[e] = __uint_as_float(v[e]);
         }
         tc_fence_before();
         mbar_arrive(&sm.s_empty);
@@ -299,14 +298,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           ++nod;
           tc_fence_after();
           if (__any_sync(0xffffffffu, resc)) {  // O holds this unit's partial sum
+            uint32_t v[64];
+            tmem_ld64(tO, v);
+            uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+            uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tO + 32 * c, v);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              tmem_st32(tO + 32 * c, v);
-            }
+            for (int e = 0; e < 64; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st32(tO, v0);
+            tmem_st32(tO + 32, v1);
           }
         }
         tmem_st32(tP, pa);
@@ -322,14 +321,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint32_t ob[32];
+      {
+        uint32_t v[64];
+        tmem_ld64(tO, v);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + 32 * c, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          ob[16 * c + e] = pack_bf16(__uint_as_float(v[2 * e]) * inv,
-                                     __uint_as_float(v[2 * e + 1]) * inv);
+        for (int e = 0; e < 32; ++e)
+          ob[e] = pack_bf16(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
       }
       if (r < u.nrows) {
         uint4* dst = reinterpret_cast<uint4*>(

@@ -36,7 +36,7 @@ struct BwdProblem {
   __nv_bfloat16* dv;
   float* dsinks;
   float* D;                    // [Hq, total] workspace: rowsum(dO * O)
-  float* sink_part;            // [Hq, part_stride, 4] workspace: per key tile and
+  float* sink_part;            // [Hq, part_stride, 8] workspace: per key tile and
                                // softmax warp, sum of p_sink * P * dP
   float* dq_acc;               // [total, Hq, 64] fp32 workspace
   int32_t nchunks;             // token chunks of the preprocess pass
