@@ -184,6 +184,8 @@ EncodeTiledFn encode_tiled() {
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+void note_error_message(const std::string& msg) { g_message = msg; }
+
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
                                 int64_t row_stride) {
   EncodeTiledFn enc = encode_tiled();

@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 namespace sinkattn {
 
@@ -94,5 +95,8 @@ cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int n
 
 // Counts kernel launches (sinkattn_launch_count).
 void note_launch(int n = 1);
+
+// Sets the calling thread's detail message (sinkattn_last_error_message).
+void note_error_message(const std::string& msg);
 
 }  // namespace sinkattn

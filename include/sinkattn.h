@@ -135,6 +135,27 @@ SINKATTN_API size_t sinkattn_bwd_workspace_size(int32_t nseq, int32_t total, int
 SINKATTN_API sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* params, void* stream);
 SINKATTN_API sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* params, void* stream);
 
+/* Backward with no caller workspace, for callers that cannot allocate device
+ * memory when they call the library: a host that has already handed the
+ * whole device to its own memory pool, or code that runs where an
+ * allocation's implicit synchronisation is not allowed. Same parameters,
+ * results and errors as sinkattn_bwd; params->workspace and workspace_bytes
+ * are ignored. The pages this library follows have no counterpart to this
+ * entry point.
+ *
+ * The scratch memory is one array inside the library of
+ * SINKATTN_STATIC_BWD_WORKSPACE_BYTES bytes, held by every GPU that loads the
+ * library until the process exits. A problem whose
+ * sinkattn_bwd_workspace_size() exceeds it returns SINKATTN_ERR_WORKSPACE and
+ * launches nothing. The array's device address is looked up on the first call
+ * made on each device (with that device current), so make that first call
+ * before any stream capture. Every call shares the array and it keeps the
+ * last call's contents (nothing in it needs to start at zero); calls that
+ * overlap on the GPU, on any stream, race on it. */
+#define SINKATTN_STATIC_BWD_WORKSPACE_BYTES ((size_t)64 << 20)
+SINKATTN_API sinkattn_status sinkattn_bwd_static_workspace(const sinkattn_bwd_params* params,
+                                                           void* stream);
+
 /* Static description of a status code; never NULL. */
 SINKATTN_API const char* sinkattn_status_string(int32_t status);
 
