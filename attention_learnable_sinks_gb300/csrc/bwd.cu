@@ -102,8 +102,9 @@ struct __align__(1024) Smem {
   uint8_t pt[2 * kTileBytes];      // P^T: two [128 keys][64 q] blocks (one per half)
   uint8_t dst[2][2 * kTileBytes];  // dS^T, double-buffered by tile parity
   uint8_t dq[kTileBytes];          // dQ staging: one [128 q][32] fp32 box
-  float4 rowinfo[kQStages][kTile];  // per query row: {LSE*log2e (+inf outside
-                                    // the sequence), D, p_sink, 0}
+  float4 rowld[kQStages][kTile / 2];  // per query-row pair: {-LSE*log2e (-inf
+                                      // outside the sequence) x2, -D x2}
+  float2 rowps[kQStages][kTile / 2];  // per query-row pair: p_sink x2
   uint64_t kv_full, kv_empty, q_full[kQStages], q_empty[kQStages];
   uint64_t sdp_full[2], sdp_empty[2], pds_full[2], p_free[2], ds_free[2];
   uint64_t dq_full, dq_empty, dkv_full, dkv_empty, stg_free, stg_full, drain;
@@ -241,13 +242,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           ok = false;
           break;
         }
+        float l2[4], dd[4], ps[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int q = q0 + lane * 4 + e;
-          const bool in = q < u.L;
-          const float l2 = in ? lv[e] * kLog2e : INFINITY;
-          sm.rowinfo[st][lane * 4 + e] =
-              make_float4(l2, in ? dv[e] : 0.f, in && p.sinks ? ex2(sink2 - l2) : 0.f, 0.f);
+          const bool in = q0 + lane * 4 + e < u.L;
+          l2[e] = in ? lv[e] * kLog2e : INFINITY;
+          dd[e] = in ? dv[e] : 0.f;
+          ps[e] = in && p.sinks ? ex2(sink2 - l2[e]) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          sm.rowld[st][lane * 2 + e / 2] = make_float4(-l2[e], -l2[e + 1], -dd[e], -dd[e + 1]);
+          sm.rowps[st][lane * 2 + e / 2] = make_float2(ps[e], ps[e + 1]);
         }
         __syncwarp();
         if (lane == 0) {
@@ -268,7 +274,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const uint32_t idS = idesc_bf16(kTile, 64, false, false);
       const uint32_t idKV = idesc_bf16(kTile, kHeadDim, false, true);
       const uint32_t idQ = idesc_bf16(kTile, kHeadDim, true, true);
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), pa = smem_u32(sm.pt);
+      // descriptors built once; a product adds its byte offset / 16
+      const uint64_t dK = sdesc_sw128(smem_u32(sm.k), 16, 1024);        // K-major
+      const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k), 8192, 1024);    // MN-major
+      const uint64_t dV = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+      const uint64_t dP = sdesc_sw128(smem_u32(sm.pt), 16, 1024);
+      static_assert(kQStages == 2, "stage descriptors below assume two stages");
+      // per-stage / per-buffer operands differ by a fixed byte distance
+      const uint64_t dQk0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dQmn0 = sdesc_sw128(smem_u32(sm.q[0]), 8192, 1024);
+      const uint64_t dOk0 = sdesc_sw128(smem_u32(sm.dout[0]), 16, 1024);
+      const uint64_t dOmn0 = sdesc_sw128(smem_u32(sm.dout[0]), 8192, 1024);
+      const uint64_t dSk0 = sdesc_sw128(smem_u32(sm.dst[0]), 16, 1024);
+      const uint64_t dSm0 = sdesc_sw128(smem_u32(sm.dst[0]), kTileBytes, 1024);
+      constexpr uint64_t kStageStep = kTileBytes >> 4;        // q[1] - q[0], dout[1] - dout[0]
+      constexpr uint64_t kDsStep = (2 * kTileBytes) >> 4;     // dst[1] - dst[0]
       uint32_t nunit = 0, ntile = 0, nsdp[2] = {0, 0}, npds[2] = {0, 0}, ndq = 0;
       bool ok = true;
       // S^T and dP^T of half hf of a query tile (its Q / dO stage must be full)
@@ -277,14 +297,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (!mbar_wait(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) return false;
         ++nsdp[hf];
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm.q[st]) + hf * kHalfBytes;
-        const uint32_t oa = smem_u32(sm.dout[st]) + hf * kHalfBytes;
+        const uint64_t bq = dQk0 + st * kStageStep + hf * (kHalfBytes >> 4);
+        const uint64_t bo = dOk0 + st * kStageStep + hf * (kHalfBytes >> 4);
 #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k) {
-          umma_ss(tmem + kColS + 64 * hf, sdesc_sw128(ka + 32 * k, 16, 1024),
-                  sdesc_sw128(qa + 32 * k, 16, 1024), idS, k > 0);
-          umma_ss(tmem + kColDP + 64 * hf, sdesc_sw128(va + 32 * k, 16, 1024),
-                  sdesc_sw128(oa + 32 * k, 16, 1024), idS, k > 0);
+        for (int k = 0; k < kHeadDim / 16; ++k) {  // +32 bytes per 16 features
+          umma_ss(tmem + kColS + 64 * hf, dK + 2 * k, bq + 2 * k, idS, k > 0);
+          umma_ss(tmem + kColDP + 64 * hf, dV + 2 * k, bo + 2 * k, idS, k > 0);
         }
         umma_commit(&sm.sdp_full[hf]);
         return true;
@@ -303,7 +321,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           const uint32_t tile = tile0 + i;
           const int st = tile % kQStages, db = tile & 1;
           const bool more = i + 1 < nt;
-          bool next_ready = false;  // Q / dO of the next tile landed
+          // S^T / dP^T of the next tile are issued right after each half's
+          // dV / dK -- if the next tile's Q / dO have landed by then;
+          // otherwise after this tile's dQ, instead of blocking here
+          bool deferred = !more;
           for (int hf = 0; hf < 2; ++hf) {
             if (!mbar_wait(&sm.pds_full[hf], npds[hf] & 1, g)) {
               ok = false;
@@ -311,25 +332,23 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             }
             ++npds[hf];
             tc_fence_after();
-            const uint32_t qa = smem_u32(sm.q[st]) + hf * kHalfBytes;
-            const uint32_t oa = smem_u32(sm.dout[st]) + hf * kHalfBytes;
-            const uint32_t da = smem_u32(sm.dst[db]) + hf * kTileBytes;
+            const uint64_t ap = dP + hf * (kTileBytes >> 4);
+            const uint64_t as = dSk0 + db * kDsStep + hf * (kTileBytes >> 4);
+            const uint64_t bo = dOmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
+            const uint64_t bq = dQmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
               const uint32_t acc = (i > 0 || hf > 0 || k > 0) ? 1u : 0u;
-              umma_ss(tmem + kColDV, sdesc_sw128(pa + hf * kTileBytes + 32 * k, 16, 1024),
-                      sdesc_sw128(oa + 2048 * k, 8192, 1024), idKV, acc);
-              umma_ss(tmem + kColDK, sdesc_sw128(da + 32 * k, 16, 1024),
-                      sdesc_sw128(qa + 2048 * k, 8192, 1024), idKV, acc);
+              umma_ss(tmem + kColDV, ap + 2 * k, bo + 128 * k, idKV, acc);  // +2048 B / 16 rows
+              umma_ss(tmem + kColDK, as + 2 * k, bq + 128 * k, idKV, acc);
             }
             umma_commit(&sm.p_free[hf]);
-            // look ahead: S^T / dP^T of the same half of the next tile, unless
-            // its Q / dO have not landed yet (then after dQ, below)
-            if (more) {
+            if (hf == 1) umma_commit(&sm.q_empty[st]);  // last reader of Q / dO
+            if (!deferred) {
               if (hf == 0)
-                next_ready = mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
-                                           ((tile + 1) / kQStages) & 1);
-              if (next_ready && !issue_sdp(tile + 1, hf)) {
+                deferred = !mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
+                                          ((tile + 1) / kQStages) & 1);
+              if (!deferred && !issue_sdp(tile + 1, hf)) {
                 ok = false;
                 break;
               }
@@ -339,15 +358,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           if (!mbar_wait(&sm.dq_empty, (ndq & 1) ^ 1, g)) break;
           ++ndq;
           tc_fence_after();
-          const uint32_t dsa = smem_u32(sm.dst[db]);
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time
-            umma_ss(tmem + kColDQ, sdesc_sw128(dsa + 2048 * k, kTileBytes, 1024),
-                    sdesc_sw128(ka + 2048 * k, 8192, 1024), idQ, k > 0);
+          for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time (+2048 B)
+            umma_ss(tmem + kColDQ, dSm0 + db * kDsStep + 128 * k, dKmn + 128 * k, idQ, k > 0);
           umma_commit(&sm.ds_free[db]);
           umma_commit(&sm.dq_full);
-          umma_commit(&sm.q_empty[st]);
-          if (more && !next_ready) {
+          if (more && deferred) {
             if (!mbar_wait(&sm.q_full[(tile + 1) % kQStages], ((tile + 1) / kQStages) & 1, g) ||
                 !issue_sdp(tile + 1, 0) || !issue_sdp(tile + 1, 1)) {
               ok = false;
@@ -372,7 +388,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + kColS + 64 * hf;
     const uint32_t tdP = tmem + lane_off + kColDP + 64 * hf;
-    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2pack(p.scale_log2, p.scale_log2);
     uint32_t nunit = 0, ntile = 0, nsd = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
@@ -381,7 +397,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const bool jvalid = r < u.nkeys;
       const int qlo = p.causal ? j : 0;
       const int qhi = p.window > 0 ? j + p.window : 0x7fffffff;
-      float sa0 = 0.f, sa1 = 0.f, sa2 = 0.f, sa3 = 0.f;
+      uint64_t sa0 = f2pack(0.f, 0.f), sa1 = f2pack(0.f, 0.f);
       for (int i = 0; i < G * u.nq && ok; ++i, ++ntile) {
         const int hh = i / u.nq;
         const int qb = (u.qt0 + i % u.nq) * kTile + 64 * hf;
@@ -396,55 +412,68 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tc_fence_after();
         const bool full = jvalid && qb >= qlo && qb + 63 < qhi;
         const int cl = qlo - qb, ch = qhi - qb;
-        const float4* info = &sm.rowinfo[st][64 * hf];
         uint8_t* prow = sm.pt + hf * kTileBytes;
         uint8_t* srow = sm.dst[db] + hf * kTileBytes;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {  // 16 query columns at a time
-          uint32_t sv[16], pv[16];
-          tmem_ld16x2(tS + 16 * c, tdP + 16 * c, sv, pv);
-          if (c == 3) {
-            tc_fence_before();
-            mbar_arrive(&sm.sdp_empty[hf]);
-          }
+        // 16 query columns at a time; the TMEM load of chunk c+1 is in flight
+        // while chunk c is computed
+        const float4* ld = &sm.rowld[st][32 * hf];
+        const float2* pp = &sm.rowps[st][32 * hf];
+        uint32_t sv[2][16], pv[2][16];
+        tmem_ld16x2_async(tS, tdP, sv[0], pv[0]);
+        tmem_ld_wait();
+        reg_fence16(sv[0]);
+        reg_fence16(pv[0]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int cur = c & 1;
+          if (c < 3) tmem_ld16x2_async(tS + 16 * (c + 1), tdP + 16 * (c + 1), sv[cur ^ 1], pv[cur ^ 1]);
           uint32_t pP[8], pS[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
             const int col = 16 * c + e;
-            const float4 i0 = info[col], i1 = info[col + 1];  // {LSE*log2e, D, p_sink, -}
-            float P0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -i0.x));
-            float P1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -i1.x));
+            const float4 a = ld[col / 2];  // {-LSE*log2e x2, -D x2}
+            const float2 b = pp[col / 2];  // p_sink x2
+            const float2 x = f2unpack(ffma2(f2pack(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])),
+                                            sl2x2, f2pack(a.x, a.y)));
+            float P0 = ex2(x.x), P1 = ex2(x.y);
             if (!full) {
               if (!jvalid || col < cl || col >= ch) P0 = 0.f;
               if (!jvalid || col + 1 < cl || col + 1 >= ch) P1 = 0.f;
             }
-            const float t0 = P0 * __uint_as_float(pv[e]);
-            const float t1 = P1 * __uint_as_float(pv[e + 1]);
-            if (e & 2) {
-              sa2 = fmaf(i0.z, t0, sa2);
-              sa3 = fmaf(i1.z, t1, sa3);
-            } else {
-              sa0 = fmaf(i0.z, t0, sa0);
-              sa1 = fmaf(i1.z, t1, sa1);
-            }
+            const uint64_t P = f2pack(P0, P1);
+            const uint64_t t = fmul2(P, f2pack(__uint_as_float(pv[cur][e]), __uint_as_float(pv[cur][e + 1])));
+            if (e & 2)
+              sa1 = ffma2(f2pack(b.x, b.y), t, sa1);
+            else
+              sa0 = ffma2(f2pack(b.x, b.y), t, sa0);
+            const float2 ds = f2unpack(ffma2(P, f2pack(a.z, a.w), t));  // P (dP - D)
             pP[e / 2] = pack_bf16(P0, P1);
-            pS[e / 2] = pack_bf16(fmaf(-P0, i0.y, t0), fmaf(-P1, i1.y, t1));
+            pS[e / 2] = pack_bf16(ds.x, ds.y);
           }
           if (c == 0) {
             // P^T half free (dV / dK of the previous tile done), and this
             // tile's dS^T buffer free (dQ of the tile before that done)
             if (!mbar_wait(&sm.p_free[hf], (ntile & 1) ^ 1, g) ||
-                !mbar_wait(&sm.ds_free[db], ((ntile >> 1) & 1) ^ 1, g)) {
+                !mbar_wait(&sm.ds_free[db], ((ntile >> 1) & 1) ^ 1, g))
               ok = false;
-              break;
+          }
+          if (ok) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              *reinterpret_cast<uint4*>(prow + sw128_offset(r, 2 * c + x)) =
+                  make_uint4(pP[4 * x], pP[4 * x + 1], pP[4 * x + 2], pP[4 * x + 3]);
+              *reinterpret_cast<uint4*>(srow + sw128_offset(r, 2 * c + x)) =
+                  make_uint4(pS[4 * x], pS[4 * x + 1], pS[4 * x + 2], pS[4 * x + 3]);
             }
           }
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            *reinterpret_cast<uint4*>(prow + sw128_offset(r, 2 * c + x)) =
-                make_uint4(pP[4 * x], pP[4 * x + 1], pP[4 * x + 2], pP[4 * x + 3]);
-            *reinterpret_cast<uint4*>(srow + sw128_offset(r, 2 * c + x)) =
-                make_uint4(pS[4 * x], pS[4 * x + 1], pS[4 * x + 2], pS[4 * x + 3]);
+          if (c < 3) {
+            tmem_ld_wait();
+            reg_fence16(sv[cur ^ 1]);
+            reg_fence16(pv[cur ^ 1]);
+            if (c == 2) {  // all of this half's S^T / dP^T is in registers
+              tc_fence_before();
+              mbar_arrive(&sm.sdp_empty[hf]);
+            }
           }
         }
         if (!ok) break;
@@ -452,13 +481,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_arrive(&sm.pds_full[hf]);
         if (i % u.nq == u.nq - 1) {
           // head hh done: this warp's share of its sink-gradient partial
-          float v = (sa0 + sa1) + (sa2 + sa3);
+          const float2 s0 = f2unpack(sa0), s1 = f2unpack(sa1);
+          float v = (s0.x + s0.y) + (s1.x + s1.y);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           if (lane == 0)
             bp.sink_part[((int64_t)(u.kvh * G + hh) * bp.part_stride + u.item) * 8 + hf * 4 +
                          quarter] = v;
-          sa0 = sa1 = sa2 = sa3 = 0.f;
+          sa0 = sa1 = f2pack(0.f, 0.f);
         }
       }
       if (!ok) break;
@@ -502,11 +532,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         ++ndq;
         tc_fence_after();
-        uint32_t a[64];
-        tmem_ld64(tmem + lane_off + kColDQ, a);
+        uint32_t a[2][32];
+        tmem_ld32(tmem + lane_off + kColDQ, a[0]);
+        tmem_ld32(tmem + lane_off + kColDQ + 32, a[1]);
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
-        const float sc = p.scale;
         for (int half = 0; half < 2 && ok; ++half, ++nstg) {
           if (issuer) {
             bulk_wait_read0();  // the previous reduce has read the staging buffer
@@ -518,10 +548,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const int e = 32 * half + 4 * c;
-            *reinterpret_cast<float4*>(sm.dq + sw128_offset(r, c)) =
-                make_float4(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc,
-                            __uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
+            const uint32_t* v = &a[half][4 * c];
+            *reinterpret_cast<uint4*>(sm.dq + sw128_offset(r, c)) = make_uint4(v[0], v[1], v[2], v[3]);
           }
           fence_async_smem();
           mbar_arrive(&sm.stg_full);
@@ -568,10 +596,12 @@ finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
   const int64_t n8 = (int64_t)p.total * p.Hq * kHeadDim / 8;
   for (int64_t e = (int64_t)blockIdx.x * kFinishThreads + threadIdx.x; e < n8;
        e += (int64_t)gridDim.x * kFinishThreads) {
+    const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
     const float4 a = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e];
     const float4 b = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e + 1];
-    reinterpret_cast<uint4*>(bp.dq)[e] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w),
-                                                    pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+    reinterpret_cast<uint4*>(bp.dq)[e] =
+        make_uint4(pack_bf16(a.x * sc, a.y * sc), pack_bf16(a.z * sc, a.w * sc),
+                   pack_bf16(b.x * sc, b.y * sc), pack_bf16(b.z * sc, b.w * sc));
   }
 }
 
