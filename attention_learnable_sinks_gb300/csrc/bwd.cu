@@ -26,9 +26,9 @@
 //   S^T  = K Q^T      [128 keys x 64 q]   SS, both K-major        -> TMEM
 //   dP^T = V dO^T     [128 keys x 64 q]   SS, both K-major        -> TMEM
 //   P^T  = exp2(S^T * scale * log2e - LSE * log2e),  dS^T = P^T (dP^T - D)
-//        (softmax warpgroup, one key row per thread; written as bf16 to
-//        128-byte-swizzled shared memory)
-//   dV  += P^T dO     A = P^T (K-major), B = dO (MN-major)         TMEM
+//        (softmax warpgroup, one key row per thread; P^T written as bf16 to
+//        tensor memory, dS^T to 128-byte-swizzled shared memory)
+//   dV  += P^T dO     A = P^T (tensor memory), B = dO (MN-major)   TMEM
 //   dK  += dS^T Q     A = dS^T (K-major), B = Q (MN-major)         TMEM
 //   dQ   = dS K       per 128-row tile: A = the same dS^T buffer read
 //        M-major, B = K (MN-major); read out by a second warpgroup, scaled
@@ -43,7 +43,8 @@
 // p_sink), warp 1 UMMA issuer, warps 4-7 / 8-11 softmax of half 0 / 1 and
 // the dV / dK epilogue, warps 12-15 dQ read-out (warps 2-3 idle). Tensor
 // memory (512 columns): S^T [0,128) as two 64-column buffers, dP^T [128,256),
-// dV [256,320), dK [320,384), dQ [384,448).
+// dV [256,320), dK [320,384), dQ [384,448), P^T [448,512) (bf16 pairs, two
+// 32-column halves). Q / dO are triple-buffered.
 #include <algorithm>
 #include <cmath>
 
@@ -91,15 +92,15 @@ constexpr int kThreads = 512;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;        // 64 rows
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
-constexpr int kQStages = 2;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
+                   kColPT = 448;
+constexpr int kQStages = 3;
 
 struct __align__(1024) Smem {
   uint8_t k[kTileBytes];
   uint8_t v[kTileBytes];
   uint8_t q[kQStages][kTileBytes];
   uint8_t dout[kQStages][kTileBytes];
-  uint8_t pt[2 * kTileBytes];      // P^T: two [128 keys][64 q] blocks (one per half)
   uint8_t dst[2][2 * kTileBytes];  // dS^T, double-buffered by tile parity
   uint8_t dq[kTileBytes];          // dQ staging: one [128 q][32] fp32 box
   float4 rowld[kQStages][kTile / 2];  // per query-row pair: {-LSE*log2e (-inf
@@ -278,8 +279,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const uint64_t dK = sdesc_sw128(smem_u32(sm.k), 16, 1024);        // K-major
       const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k), 8192, 1024);    // MN-major
       const uint64_t dV = sdesc_sw128(smem_u32(sm.v), 16, 1024);
-      const uint64_t dP = sdesc_sw128(smem_u32(sm.pt), 16, 1024);
-      static_assert(kQStages == 2, "stage descriptors below assume two stages");
       // per-stage / per-buffer operands differ by a fixed byte distance
       const uint64_t dQk0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t dQmn0 = sdesc_sw128(smem_u32(sm.q[0]), 8192, 1024);
@@ -321,30 +320,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           const uint32_t tile = tile0 + i;
           const int st = tile % kQStages, db = tile & 1;
           const bool more = i + 1 < nt;
-          // S^T / dP^T of the next tile are issued right after each half's
-          // dV / dK -- if the next tile's Q / dO have landed by then;
-          // otherwise after this tile's dQ, instead of blocking here
+          // S^T / dP^T of the same half of the next tile go in as soon as this
+          // half's softmax has read its buffer (before this half's dV / dK),
+          // if the next tile's Q / dO have landed; otherwise after this dQ
           bool deferred = !more;
           for (int hf = 0; hf < 2; ++hf) {
-            if (!mbar_wait(&sm.pds_full[hf], npds[hf] & 1, g)) {
-              ok = false;
-              break;
-            }
-            ++npds[hf];
-            tc_fence_after();
-            const uint64_t ap = dP + hf * (kTileBytes >> 4);
-            const uint64_t as = dSk0 + db * kDsStep + hf * (kTileBytes >> 4);
-            const uint64_t bo = dOmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
-            const uint64_t bq = dQmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
-              const uint32_t acc = (i > 0 || hf > 0 || k > 0) ? 1u : 0u;
-              umma_ss(tmem + kColDV, ap + 2 * k, bo + 128 * k, idKV, acc);  // +2048 B / 16 rows
-              umma_ss(tmem + kColDK, as + 2 * k, bq + 128 * k, idKV, acc);
-            }
-            umma_commit(&sm.p_free[hf]);
-            if (hf == 1) umma_commit(&sm.q_empty[st]);  // last reader of Q / dO
             if (!deferred) {
+              if (!mbar_wait(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) {
+                ok = false;
+                break;
+              }
               if (hf == 0)
                 deferred = !mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
                                           ((tile + 1) / kQStages) & 1);
@@ -353,6 +338,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 break;
               }
             }
+            if (!mbar_wait(&sm.pds_full[hf], npds[hf] & 1, g)) {
+              ok = false;
+              break;
+            }
+            ++npds[hf];
+            tc_fence_after();
+            const uint32_t ap = tmem + kColPT + 32 * hf;  // P^T of this half (TMEM)
+            const uint64_t as = dSk0 + db * kDsStep + hf * (kTileBytes >> 4);
+            const uint64_t bo = dOmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
+            const uint64_t bq = dQmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
+              const uint32_t acc = (i > 0 || hf > 0 || k > 0) ? 1u : 0u;
+              umma_ts(tmem + kColDV, ap + 8 * k, bo + 128 * k, idKV, acc);  // +2048 B / 16 rows
+              umma_ss(tmem + kColDK, as + 2 * k, bq + 128 * k, idKV, acc);
+            }
+            umma_commit(&sm.p_free[hf]);
+            if (hf == 1) umma_commit(&sm.q_empty[st]);  // last reader of Q / dO
           }
           if (!ok) break;
           if (!mbar_wait(&sm.dq_empty, (ndq & 1) ^ 1, g)) break;
@@ -412,7 +415,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tc_fence_after();
         const bool full = jvalid && qb >= qlo && qb + 63 < qhi;
         const int cl = qlo - qb, ch = qhi - qb;
-        uint8_t* prow = sm.pt + hf * kTileBytes;
+        const uint32_t tPT = tmem + lane_off + kColPT + 32 * hf;
         uint8_t* srow = sm.dst[db] + hf * kTileBytes;
         // 16 query columns at a time; the TMEM load of chunk c+1 is in flight
         // while chunk c is computed
@@ -457,14 +460,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 !mbar_wait(&sm.ds_free[db], ((ntile >> 1) & 1) ^ 1, g))
               ok = false;
           }
+          // P^T (bf16 pairs) to tensor memory -- warp-wide, so always issued;
+          // dS^T to shared memory
+          tmem_st8(tPT + 8 * c, pP);
           if (ok) {
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              *reinterpret_cast<uint4*>(prow + sw128_offset(r, 2 * c + x)) =
-                  make_uint4(pP[4 * x], pP[4 * x + 1], pP[4 * x + 2], pP[4 * x + 3]);
+            for (int x = 0; x < 2; ++x)
               *reinterpret_cast<uint4*>(srow + sw128_offset(r, 2 * c + x)) =
                   make_uint4(pS[4 * x], pS[4 * x + 1], pS[4 * x + 2], pS[4 * x + 3]);
-            }
           }
           if (c < 3) {
             tmem_ld_wait();
@@ -476,8 +479,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             }
           }
         }
+        tmem_st_wait();
         if (!ok) break;
         fence_async_smem();
+        tc_fence_before();
         mbar_arrive(&sm.pds_full[hf]);
         if (i % u.nq == u.nq - 1) {
           // head hh done: this warp's share of its sink-gradient partial
