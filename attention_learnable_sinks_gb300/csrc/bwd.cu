@@ -60,31 +60,36 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kPrepThreads = 256;
 
 // ---------------------------------------------------------------- preprocess
+// One warp per four (token, head) rows, 16 bytes per lane: D = rowsum(dO * O)
+// reduced over the row's eight lanes, and the row's 256 bytes of the fp32 dq
+// accumulator cleared with coalesced stores.
 __global__ void __launch_bounds__(kPrepThreads)
 preprocess_kernel(BwdProblem bp) {
   const Problem& p = bp.f;
-  const int64_t row = (int64_t)blockIdx.x * kPrepThreads + threadIdx.x;  // token * Hq + head
-  if (row >= (int64_t)p.total * p.Hq) return;
-  const int64_t t = row / p.Hq;
-  const int h = (int)(row % p.Hq);
-  const uint4* o4 = reinterpret_cast<const uint4*>(p.o + row * kHeadDim);
-  const uint4* g4 = reinterpret_cast<const uint4*>(bp.dout + row * kHeadDim);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * kPrepThreads + threadIdx.x) >> 5;
+  const int64_t row = warp_id * 4 + (lane >> 3);  // token * Hq + head
+  const int sub = lane & 7;                       // 16-byte chunk of the row
+  const bool in = row < (int64_t)p.total * p.Hq;
   float D = 0.f;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 a = o4[c], b = g4[c];
+  if (in) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p.o + row * kHeadDim + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(bp.dout + row * kHeadDim + sub * 8);
     const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(b2[e]);
-      D += x.x * y.x + x.y * y.y;
+      D = fmaf(x.x, y.x, fmaf(x.y, y.y, D));
     }
+    float4* acc = reinterpret_cast<float4*>(bp.dq_acc + row * kHeadDim) + sub * 2;
+    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  bp.D[(int64_t)h * p.total + t] = D;
-  float4* acc = reinterpret_cast<float4*>(bp.dq_acc + row * kHeadDim);
-#pragma unroll
-  for (int c = 0; c < 16; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  D += __shfl_xor_sync(0xffffffffu, D, 1);
+  D += __shfl_xor_sync(0xffffffffu, D, 2);
+  D += __shfl_xor_sync(0xffffffffu, D, 4);
+  if (in && sub == 0) bp.D[(row % p.Hq) * p.total + row / p.Hq] = D;
 }
 
 // ---------------------------------------------------------------- main
@@ -599,8 +604,8 @@ finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
     }
   }
   const int64_t n8 = (int64_t)p.total * p.Hq * kHeadDim / 8;
-  for (int64_t e = (int64_t)blockIdx.x * kFinishThreads + threadIdx.x; e < n8;
-       e += (int64_t)gridDim.x * kFinishThreads) {
+  const int64_t e = (int64_t)blockIdx.x * kFinishThreads + threadIdx.x;  // 8 elements each
+  if (e < n8) {
     const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
     const float4 a = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e];
     const float4 b = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e + 1];
@@ -615,8 +620,9 @@ finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
 cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s) {
   const int64_t rows = (int64_t)p.f.total * p.f.Hq;
   if (rows == 0) return cudaSuccess;
-  preprocess_kernel<<<(unsigned)((rows + kPrepThreads - 1) / kPrepThreads), kPrepThreads, 0, s>>>(
-      p);
+  const int64_t rows_per_block = kPrepThreads / 8;  // four rows per warp
+  preprocess_kernel<<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), kPrepThreads, 0,
+                      s>>>(p);
   note_launch();
   return cudaGetLastError();
 }
@@ -645,9 +651,9 @@ cudaError_t launch_bwd_main(const BwdProblem& p, const TileList& ktiles, int num
 
 cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int num_sms,
                               cudaStream_t s) {
+  (void)num_sms;
   const int64_t n8 = (int64_t)p.f.total * p.f.Hq * kHeadDim / 8;
-  const int64_t blocks = std::max<int64_t>(
-      1, std::min<int64_t>((n8 + kFinishThreads - 1) / kFinishThreads, (int64_t)num_sms * 8));
+  const int64_t blocks = std::max<int64_t>(1, (n8 + kFinishThreads - 1) / kFinishThreads);
   finish_kernel<<<(unsigned)blocks, kFinishThreads, 0, s>>>(p, ktiles.meta);
   note_launch();
   return cudaGetLastError();
