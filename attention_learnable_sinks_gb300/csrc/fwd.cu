@@ -13,7 +13,9 @@
 // with the other's matrix products.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer: Q tile, then K/V tiles into a 2-stage ring
+//   warp 0      TMA producer: Q tile, then K tiles (3-stage ring, one tile
+//               ahead) and V tiles (2-stage ring); a K stage is released as
+//               soon as S = Q K^T completes, a V stage after O += P V
 //   warp 1      UMMA issuer: S = Q K^T (SS, K-major both) and O += P V (P from
 //               tensor memory, V MN-major); S(j+1) is issued as soon as the
 //               softmax has read S(j), so it overlaps softmax(j)
@@ -34,7 +36,8 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB of bf16
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
@@ -44,10 +47,10 @@ constexpr float kRescale = 8.0f;  // log2 units
 
 struct __align__(1024) Smem {
   uint8_t q[kTileBytes];
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint8_t k[kKStages][kTileBytes];
+  uint8_t v[kVStages][kTileBytes];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t q_full, q_empty, s_full, s_empty, p_full, o_done, drain;
   uint32_t tmem_base;
   int abort;
@@ -95,9 +98,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
@@ -125,30 +132,43 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t nq = 0, nkv = 0;
+      uint32_t nq = 0, nk = 0, nv = 0;
+      auto load_k = [&](const Unit& u, int kt) -> bool {
+        const int s = nk % kKStages;
+        if (!mbar_wait(&sm.k_empty[s], ((nk / kKStages) & 1) ^ 1, g)) return false;
+        mbar_expect_tx(&sm.k_full[s], kTileBytes);
+        tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, u.kvh, u.base + kt * kTile);
+        ++nk;
+        return true;
+      };
+      auto load_v = [&](const Unit& u, int kt) -> bool {
+        const int s = nv % kVStages;
+        if (!mbar_wait(&sm.v_empty[s], ((nv / kVStages) & 1) ^ 1, g)) return false;
+        mbar_expect_tx(&sm.v_full[s], kTileBytes);
+        tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, u.kvh, u.base + kt * kTile);
+        ++nv;
+        return true;
+      };
       for (int w = blockIdx.x; w < nwork; w += gridDim.x) {
         const Unit u = decode(p, items, w);
         if (!mbar_wait(&sm.q_empty, (nq & 1) ^ 1, g)) break;
         mbar_expect_tx(&sm.q_full, kTileBytes);
         tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base + u.r0);
         ++nq;
-        bool ok = true;
-        for (int kt = u.kt0; kt < u.kt1; ++kt, ++nkv) {
-          const int s = nkv % kStages;
-          if (!mbar_wait(&sm.kv_empty[s], ((nkv / kStages) & 1) ^ 1, g)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&sm.kv_full[s], 2 * kTileBytes);
-          tma_load_3d(sm.k[s], &tm_k, &sm.kv_full[s], 0, u.kvh, u.base + kt * kTile);
-          tma_load_3d(sm.v[s], &tm_v, &sm.kv_full[s], 0, u.kvh, u.base + kt * kTile);
+        // K runs one tile ahead of V (S(j+1) is issued before P V(j))
+        bool ok = load_k(u, u.kt0);
+        for (int kt = u.kt0; kt < u.kt1 && ok; ++kt) {
+          if (kt + 1 < u.kt1) ok = load_k(u, kt + 1);
+          if (ok) ok = load_v(u, kt);
         }
         if (!ok) break;
       }
       if (g.aborted()) {  // let issued copies land before the CTA exits
         if (nq) drain_wait(&sm.q_full, (nq - 1) & 1);
-        for (uint32_t c = nkv > kStages ? nkv - kStages : 0; c < nkv; ++c)
-          drain_wait(&sm.kv_full[c % kStages], (c / kStages) & 1);
+        for (uint32_t c = nk > kKStages ? nk - kKStages : 0; c < nk; ++c)
+          drain_wait(&sm.k_full[c % kKStages], (c / kKStages) & 1);
+        for (uint32_t c = nv > kVStages ? nv - kVStages : 0; c < nv; ++c)
+          drain_wait(&sm.v_full[c % kVStages], (c / kVStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -157,7 +177,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const uint32_t idS = idesc_bf16(kTile, kTile, false, false);
       const uint32_t idO = idesc_bf16(kTile, kHeadDim, false, true);
       const uint32_t qa = smem_u32(sm.q);
-      uint32_t nq = 0, nkv = 0, ns = 0, np = 0;
+      uint32_t nq = 0, nk = 0, ns = 0, np = 0;
       auto issue_s = [&](int s) {
         const uint32_t ka = smem_u32(sm.k[s]);
 #pragma unroll
@@ -173,46 +193,47 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                   idO, acc || k > 0);
       };
       bool ok = true;
+      // S of the next key tile (K stage released when it completes)
+      auto next_s = [&]() -> bool {
+        const int s = nk % kKStages;
+        if (!mbar_wait(&sm.k_full[s], (nk / kKStages) & 1, g) ||
+            !mbar_wait(&sm.s_empty, (ns & 1) ^ 1, g))
+          return false;
+        ++ns;
+        tc_fence_after();
+        issue_s(s);
+        umma_commit(&sm.s_full);
+        umma_commit(&sm.k_empty[s]);
+        ++nk;
+        return true;
+      };
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
         const Unit u = decode(p, items, w);
         const int n = u.kt1 - u.kt0;
         if (!mbar_wait(&sm.q_full, nq & 1, g)) break;
         ++nq;
-        // S(0)
-        const uint32_t first = nkv;
-        if (!mbar_wait(&sm.kv_full[first % kStages], (first / kStages) & 1, g)) break;
-        if (!mbar_wait(&sm.s_empty, (ns & 1) ^ 1, g)) break;
-        ++ns;
-        tc_fence_after();
-        issue_s(first % kStages);
-        umma_commit(&sm.s_full);
+        if (!next_s()) break;
         if (n == 1) umma_commit(&sm.q_empty);
         for (int jj = 0; jj < n; ++jj) {
-          const uint32_t cur = first + jj;
           if (jj + 1 < n) {
-            const uint32_t nxt = cur + 1;
-            if (!mbar_wait(&sm.kv_full[nxt % kStages], (nxt / kStages) & 1, g) ||
-                !mbar_wait(&sm.s_empty, (ns & 1) ^ 1, g)) {
+            if (!next_s()) {
               ok = false;
               break;
             }
-            ++ns;
-            tc_fence_after();
-            issue_s(nxt % kStages);
-            umma_commit(&sm.s_full);
             if (jj + 2 == n) umma_commit(&sm.q_empty);
           }
-          if (!mbar_wait(&sm.p_full, np & 1, g)) {
+          const int sv = np % kVStages;
+          if (!mbar_wait(&sm.p_full, np & 1, g) ||
+              !mbar_wait(&sm.v_full[sv], (np / kVStages) & 1, g)) {
             ok = false;
             break;
           }
           ++np;
           tc_fence_after();
-          issue_pv(cur % kStages, jj > 0);
-          umma_commit(&sm.kv_empty[cur % kStages]);
+          issue_pv(sv, jj > 0);
+          umma_commit(&sm.v_empty[sv]);
           umma_commit(&sm.o_done);
         }
-        nkv = first + n;
       }
       umma_commit(&sm.drain);  // every product issued above has completed
       drain_wait(&sm.drain, 0);
