@@ -20,8 +20,8 @@
 //               the partials)
 //
 // Main kernel. One CTA per SM owns a 128-key tile of one kv head at a time
-// (persistent, static round robin over the device-built key-tile list,
-// longest first) and loops over the G query heads of the group x the
+// (persistent; units are taken dynamically from the device-built key-tile
+// list, longest first) and loops over the G query heads of the group x the
 // 128-row query tiles that see the key tile, each split in two 64-row halves:
 //   S^T  = K Q^T      [128 keys x 64 q]   SS, both K-major        -> TMEM
 //   dP^T = V dO^T     [128 keys x 64 q]   SS, both K-major        -> TMEM
@@ -100,6 +100,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
                    kColPT = 448;
 constexpr int kQStages = 3;
+constexpr int kSchedSlots = 4;
+// consumers of a scheduler slot: the UMMA thread, 8 softmax warps, 4 dQ warps
+constexpr int kSchedConsumers = 1 + 8 + 4;
 
 struct __align__(1024) Smem {
   uint8_t k[kTileBytes];
@@ -114,6 +117,8 @@ struct __align__(1024) Smem {
   uint64_t kv_full, kv_empty, q_full[kQStages], q_empty[kQStages];
   uint64_t sdp_full[2], sdp_empty[2], pds_full[2], p_free[2], ds_free[2];
   uint64_t dq_full, dq_empty, dkv_full, dkv_empty, stg_free, stg_full, drain;
+  uint64_t sched_full[kSchedSlots], sched_empty[kSchedSlots];
+  int32_t sched_unit[kSchedSlots];  // work unit handed out, -1 = no more work
   uint32_t tmem_base;
   int abort;
 };
@@ -138,6 +143,23 @@ __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int 
   u.qt0 = lo / kTile;
   u.nq = (hi + kTile - 1) / kTile - u.qt0;
   return u;
+}
+
+// Work units are handed out dynamically (longest first, from the device-built
+// list): the producer warp takes the next index with an atomic and publishes
+// it in a small ring; every other role reads the ring in order.
+// `lanes` = the calling lanes of the warp (all of them read the slot before
+// the arriving lane releases it).
+template <class SmemT>
+__device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g, bool arrive,
+                                         unsigned lanes) {
+  const int s = n % kSchedSlots;
+  if (!mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g)) return -1;
+  const int w = sm.sched_unit[s];
+  __syncwarp(lanes);
+  if (arrive) mbar_arrive(&sm.sched_empty[s]);
+  ++n;
+  return w;
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -168,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
            const __grid_constant__ CUtensorMap tm_dq, BwdProblem bp,
-           const int2* __restrict__ items, const int32_t* __restrict__ meta) {
+           const int2* __restrict__ items, int32_t* __restrict__ meta) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -198,6 +220,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     mbar_init(&sm.stg_free, 1);
     mbar_init(&sm.stg_full, 128);
     mbar_init(&sm.drain, 1);
+    for (int s = 0; s < kSchedSlots; ++s) {
+      mbar_init(&sm.sched_full[s], 1);
+      mbar_init(&sm.sched_empty[s], kSchedConsumers);
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -219,9 +245,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t nunit = 0, ntile = 0;
+    uint32_t nunit = 0, ntile = 0, nsched = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+    for (;;) {
+      // take the next unit and publish it (or -1 when the list is exhausted)
+      int w = 0;
+      if (lane == 0) w = atomicAdd(&meta[1], 1);
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w >= nwork) w = -1;
+      {
+        const int s = nsched % kSchedSlots;
+        if (!mbar_wait(&sm.sched_empty[s], ((nsched / kSchedSlots) & 1) ^ 1, g)) break;
+        if (lane == 0) {
+          sm.sched_unit[s] = w;
+          mbar_arrive(&sm.sched_full[s]);
+        }
+        ++nsched;
+      }
+      if (w < 0) break;
       const Unit u = decode(p, items, w);
       if (!mbar_wait(&sm.kv_empty, (nunit & 1) ^ 1, g)) break;
       if (lane == 0) {
@@ -311,7 +352,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         umma_commit(&sm.sdp_full[hf]);
         return true;
       };
-      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+      uint32_t nsched = 0;
+      for (;;) {
+        const int w = next_unit(sm, nsched, g, true, 1u);  // lane 0 alone
+        if (w < 0) break;
         const Unit u = decode(p, items, w);
         const int nt = G * u.nq;
         if (!mbar_wait(&sm.kv_full, nunit & 1, g)) break;
@@ -397,9 +441,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t tS = tmem + lane_off + kColS + 64 * hf;
     const uint32_t tdP = tmem + lane_off + kColDP + 64 * hf;
     const uint64_t sl2x2 = f2pack(p.scale_log2, p.scale_log2);
-    uint32_t nunit = 0, ntile = 0, nsd = 0;
+    uint32_t nunit = 0, ntile = 0, nsd = 0, nsched = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+    while (ok) {
+      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
+      if (w < 0) break;
       const Unit u = decode(p, items, w);
       const int j = u.c0 + r;  // local key index
       const bool jvalid = r < u.nkeys;
@@ -529,9 +575,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool issuer = threadIdx.x == 12 * 32;
-    uint32_t ndq = 0, nstg = 0;
+    uint32_t ndq = 0, nstg = 0, nsched = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+    while (ok) {
+      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
+      if (w < 0) break;
       const Unit u = decode(p, items, w);
       for (int i = 0; i < G * u.nq; ++i) {
         const int h = u.kvh * G + i / u.nq;
