@@ -6,10 +6,10 @@
 // "GPT-OSS Agentic RL Training: A Practical Retrospective", section "The Role
 // of Attention Sinks").
 //
-// One CTA owns one 128-row query tile of one head at a time (persistent,
-// static round robin over the device-built tile list, longest first; the
-// heads of a tile are consecutive work units, so a GQA group's K/V tiles are
-// reused from L2). Two CTAs share an SM, which interleaves one CTA's softmax
+// One CTA owns one 128-row query tile of one head at a time (persistent;
+// units are taken dynamically from the device-built tile list, longest first;
+// the heads of a tile are consecutive work units, so a GQA group's K/V tiles
+// are reused from L2). Two CTAs share an SM, which interleaves one CTA's softmax
 // with the other's matrix products.
 //
 // Warp roles (192 threads):
@@ -44,6 +44,8 @@ constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;  // log2 units
+constexpr int kSchedSlots = 4;
+constexpr int kSchedConsumers = 1 + 4;  // the UMMA thread and 4 softmax warps
 
 struct __align__(1024) Smem {
   uint8_t q[kTileBytes];
@@ -52,6 +54,8 @@ struct __align__(1024) Smem {
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t q_full, q_empty, s_full, s_empty, p_full, o_done, drain;
+  uint64_t sched_full[kSchedSlots], sched_empty[kSchedSlots];
+  int32_t sched_unit[kSchedSlots];  // work unit handed out, -1 = no more work
   uint32_t tmem_base;
   int abort;
 };
@@ -78,6 +82,22 @@ __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int 
   return u;
 }
 
+// Work units are handed out dynamically (longest first, from the device-built
+// list): the producer thread takes the next index with an atomic and
+// publishes it in a small ring; the UMMA thread and the softmax warps read the
+// ring in order. `lanes` = the calling lanes of the warp.
+template <class SmemT>
+__device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g, bool arrive,
+                                         unsigned lanes) {
+  const int s = n % kSchedSlots;
+  if (!mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g)) return -1;
+  const int w = sm.sched_unit[s];
+  __syncwarp(lanes);
+  if (arrive) mbar_arrive(&sm.sched_empty[s]);
+  ++n;
+  return w;
+}
+
 // Wait that ignores the abort flag (still time-bounded): used only to drain
 // copies / products this thread issued before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -89,7 +109,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, Problem p, const int2* __restrict__ items,
-           const int32_t* __restrict__ meta) {
+           int32_t* __restrict__ meta) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -113,6 +133,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     mbar_init(&sm.p_full, 128);
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.drain, 1);
+    for (int s = 0; s < kSchedSlots; ++s) {
+      mbar_init(&sm.sched_full[s], 1);
+      mbar_init(&sm.sched_empty[s], kSchedConsumers);
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -149,7 +173,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         ++nv;
         return true;
       };
-      for (int w = blockIdx.x; w < nwork; w += gridDim.x) {
+      uint32_t nsched = 0;
+      for (;;) {
+        // take the next unit and publish it (or -1 when the list is exhausted)
+        int w = atomicAdd(&meta[1], 1);
+        if (w >= nwork) w = -1;
+        const int s = nsched % kSchedSlots;
+        if (!mbar_wait(&sm.sched_empty[s], ((nsched / kSchedSlots) & 1) ^ 1, g)) break;
+        sm.sched_unit[s] = w;
+        mbar_arrive(&sm.sched_full[s]);
+        ++nsched;
+        if (w < 0) break;
         const Unit u = decode(p, items, w);
         if (!mbar_wait(&sm.q_empty, (nq & 1) ^ 1, g)) break;
         mbar_expect_tx(&sm.q_full, kTileBytes);
@@ -207,7 +241,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         ++nk;
         return true;
       };
-      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+      uint32_t nsched = 0;
+      while (ok) {
+        const int w = next_unit(sm, nsched, g, true, 1u);  // lane 0 alone
+        if (w < 0) break;
         const Unit u = decode(p, items, w);
         const int n = u.kt1 - u.kt0;
         if (!mbar_wait(&sm.q_full, nq & 1, g)) break;
@@ -246,9 +283,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t tS = tmem + lane_off + kColS, tP = tmem + lane_off + kColP,
                    tO = tmem + lane_off + kColO;
     const float sl2 = p.scale_log2;
-    uint32_t nsf = 0, nod = 0;
+    uint32_t nsf = 0, nod = 0, nsched = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+    while (ok) {
+      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
+      if (w < 0) break;
       const Unit u = decode(p, items, w);
       const int n = u.kt1 - u.kt0;
       const int i = u.r0 + r;
