@@ -149,12 +149,12 @@ __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int 
 // list): the producer warp takes the next index with an atomic and publishes
 // it in a small ring; every other role reads the ring in order.
 // `lanes` = the calling lanes of the warp (all of them read the slot before
-// the arriving lane releases it).
+// the arriving lane releases it; all of them get the same verdict).
 template <class SmemT>
 __device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g, bool arrive,
                                          unsigned lanes) {
   const int s = n % kSchedSlots;
-  if (!mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g)) return -1;
+  if (!__all_sync(lanes, mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g))) return -1;
   const int w = sm.sched_unit[s];
   __syncwarp(lanes);
   if (arrive) mbar_arrive(&sm.sched_empty[s]);
@@ -192,8 +192,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
            const __grid_constant__ CUtensorMap tm_dq, BwdProblem bp,
            const int2* __restrict__ items, int32_t* __restrict__ meta) {
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~uintptr_t(1023));
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
   const Problem& p = bp.f;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Guard g{&sm.abort, p.err};
@@ -317,120 +316,123 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
-    if (lane == 0) {
-      const uint32_t idS = idesc_bf16(kTile, 64, false, false);
-      const uint32_t idKV = idesc_bf16(kTile, kHeadDim, false, true);
-      const uint32_t idQ = idesc_bf16(kTile, kHeadDim, true, true);
-      // descriptors built once; a product adds its byte offset / 16
-      const uint64_t dK = sdesc_sw128(smem_u32(sm.k), 16, 1024);        // K-major
-      const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k), 8192, 1024);    // MN-major
-      const uint64_t dV = sdesc_sw128(smem_u32(sm.v), 16, 1024);
-      // per-stage / per-buffer operands differ by a fixed byte distance
-      const uint64_t dQk0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
-      const uint64_t dQmn0 = sdesc_sw128(smem_u32(sm.q[0]), 8192, 1024);
-      const uint64_t dOk0 = sdesc_sw128(smem_u32(sm.dout[0]), 16, 1024);
-      const uint64_t dOmn0 = sdesc_sw128(smem_u32(sm.dout[0]), 8192, 1024);
-      const uint64_t dSk0 = sdesc_sw128(smem_u32(sm.dst[0]), 16, 1024);
-      const uint64_t dSm0 = sdesc_sw128(smem_u32(sm.dst[0]), kTileBytes, 1024);
-      constexpr uint64_t kStageStep = kTileBytes >> 4;        // q[1] - q[0], dout[1] - dout[0]
-      constexpr uint64_t kDsStep = (2 * kTileBytes) >> 4;     // dst[1] - dst[0]
-      uint32_t nunit = 0, ntile = 0, nsdp[2] = {0, 0}, npds[2] = {0, 0}, ndq = 0;
-      bool ok = true;
-      // S^T and dP^T of half hf of a query tile (its Q / dO stage must be full)
-      auto issue_sdp = [&](uint32_t tile, int hf) -> bool {
-        const int st = tile % kQStages;
-        if (!mbar_wait(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) return false;
-        ++nsdp[hf];
-        tc_fence_after();
-        const uint64_t bq = dQk0 + st * kStageStep + hf * (kHalfBytes >> 4);
-        const uint64_t bo = dOk0 + st * kStageStep + hf * (kHalfBytes >> 4);
+    // The whole warp runs this loop (uniform control flow and operands); one
+    // elected lane issues each product and commit.
+    const uint32_t idS = idesc_bf16(kTile, 64, false, false);
+    const uint32_t idKV = idesc_bf16(kTile, kHeadDim, false, true);
+    const uint32_t idQ = idesc_bf16(kTile, kHeadDim, true, true);
+    // descriptors built once; a product adds its byte offset / 16
+    const uint64_t dK = sdesc_sw128(smem_u32(sm.k), 16, 1024);        // K-major
+    const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k), 8192, 1024);    // MN-major
+    const uint64_t dV = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+    // per-stage / per-buffer operands differ by a fixed byte distance
+    const uint64_t dQk0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+    const uint64_t dQmn0 = sdesc_sw128(smem_u32(sm.q[0]), 8192, 1024);
+    const uint64_t dOk0 = sdesc_sw128(smem_u32(sm.dout[0]), 16, 1024);
+    const uint64_t dOmn0 = sdesc_sw128(smem_u32(sm.dout[0]), 8192, 1024);
+    const uint64_t dSk0 = sdesc_sw128(smem_u32(sm.dst[0]), 16, 1024);
+    const uint64_t dSm0 = sdesc_sw128(smem_u32(sm.dst[0]), kTileBytes, 1024);
+    constexpr uint64_t kStageStep = kTileBytes >> 4;        // q[1] - q[0], dout[1] - dout[0]
+    constexpr uint64_t kDsStep = (2 * kTileBytes) >> 4;     // dst[1] - dst[0]
+    uint32_t nunit = 0, ntile = 0, nsdp[2] = {0, 0}, npds[2] = {0, 0}, ndq = 0;
+    bool ok = true;
+    // S^T and dP^T of half hf of a query tile (its Q / dO stage must be full)
+    auto issue_sdp = [&](uint32_t tile, int hf) -> bool {
+      const int st = tile % kQStages;
+      if (!mbar_wait_warp(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) return false;
+      ++nsdp[hf];
+      tc_fence_after();
+      const uint64_t bq = dQk0 + st * kStageStep + hf * (kHalfBytes >> 4);
+      const uint64_t bo = dOk0 + st * kStageStep + hf * (kHalfBytes >> 4);
 #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k) {  // +32 bytes per 16 features
-          umma_ss(tmem + kColS + 64 * hf, dK + 2 * k, bq + 2 * k, idS, k > 0);
-          umma_ss(tmem + kColDP + 64 * hf, dV + 2 * k, bo + 2 * k, idS, k > 0);
-        }
-        umma_commit(&sm.sdp_full[hf]);
-        return true;
-      };
-      uint32_t nsched = 0;
-      for (;;) {
-        const int w = next_unit(sm, nsched, g, true, 1u);  // lane 0 alone
-        if (w < 0) break;
-        const Unit u = decode(p, items, w);
-        const int nt = G * u.nq;
-        if (!mbar_wait(&sm.kv_full, nunit & 1, g)) break;
-        if (!mbar_wait(&sm.dkv_empty, (nunit & 1) ^ 1, g)) break;
-        ++nunit;
-        const uint32_t tile0 = ntile;
-        if (!mbar_wait(&sm.q_full[tile0 % kQStages], (tile0 / kQStages) & 1, g) ||
-            !issue_sdp(tile0, 0) || !issue_sdp(tile0, 1))
-          break;
-        for (int i = 0; i < nt && ok; ++i) {
-          const uint32_t tile = tile0 + i;
-          const int st = tile % kQStages, db = tile & 1;
-          const bool more = i + 1 < nt;
-          // S^T / dP^T of the same half of the next tile go in as soon as this
-          // half's softmax has read its buffer (before this half's dV / dK),
-          // if the next tile's Q / dO have landed; otherwise after this dQ
-          bool deferred = !more;
-          for (int hf = 0; hf < 2; ++hf) {
-            if (!deferred) {
-              if (!mbar_wait(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) {
-                ok = false;
-                break;
-              }
-              if (hf == 0)
-                deferred = !mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
-                                          ((tile + 1) / kQStages) & 1);
-              if (!deferred && !issue_sdp(tile + 1, hf)) {
-                ok = false;
-                break;
-              }
-            }
-            if (!mbar_wait(&sm.pds_full[hf], npds[hf] & 1, g)) {
-              ok = false;
-              break;
-            }
-            ++npds[hf];
-            tc_fence_after();
-            const uint32_t ap = tmem + kColPT + 32 * hf;  // P^T of this half (TMEM)
-            const uint64_t as = dSk0 + db * kDsStep + hf * (kTileBytes >> 4);
-            const uint64_t bo = dOmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
-            const uint64_t bq = dQmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
-              const uint32_t acc = (i > 0 || hf > 0 || k > 0) ? 1u : 0u;
-              umma_ts(tmem + kColDV, ap + 8 * k, bo + 128 * k, idKV, acc);  // +2048 B / 16 rows
-              umma_ss(tmem + kColDK, as + 2 * k, bq + 128 * k, idKV, acc);
-            }
-            umma_commit(&sm.p_free[hf]);
-            if (hf == 1) umma_commit(&sm.q_empty[st]);  // last reader of Q / dO
-          }
-          if (!ok) break;
-          if (!mbar_wait(&sm.dq_empty, (ndq & 1) ^ 1, g)) break;
-          ++ndq;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time (+2048 B)
-            umma_ss(tmem + kColDQ, dSm0 + db * kDsStep + 128 * k, dKmn + 128 * k, idQ, k > 0);
-          umma_commit(&sm.ds_free[db]);
-          umma_commit(&sm.dq_full);
-          if (more && deferred) {
-            if (!mbar_wait(&sm.q_full[(tile + 1) % kQStages], ((tile + 1) / kQStages) & 1, g) ||
-                !issue_sdp(tile + 1, 0) || !issue_sdp(tile + 1, 1)) {
-              ok = false;
-              break;
-            }
-          }
-        }
-        ntile = tile0 + nt;
-        if (!ok) break;
-        umma_commit(&sm.dkv_full);
-        umma_commit(&sm.kv_empty);
+      for (int k = 0; k < kHeadDim / 16; ++k) {  // +32 bytes per 16 features
+        umma_ss_warp(tmem + kColS + 64 * hf, dK + 2 * k, bq + 2 * k, idS, k > 0);
+        umma_ss_warp(tmem + kColDP + 64 * hf, dV + 2 * k, bo + 2 * k, idS, k > 0);
       }
-      umma_commit(&sm.drain);
-      drain_wait(&sm.drain, 0);
+      umma_commit_warp(&sm.sdp_full[hf]);
+      return true;
+    };
+    uint32_t nsched = 0;
+    for (;;) {
+      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
+      if (w < 0) break;
+      const Unit u = decode(p, items, w);
+      const int nt = G * u.nq;
+      if (!mbar_wait_warp(&sm.kv_full, nunit & 1, g)) break;
+      if (!mbar_wait_warp(&sm.dkv_empty, (nunit & 1) ^ 1, g)) break;
+      ++nunit;
+      const uint32_t tile0 = ntile;
+      if (!mbar_wait_warp(&sm.q_full[tile0 % kQStages], (tile0 / kQStages) & 1, g) ||
+          !issue_sdp(tile0, 0) || !issue_sdp(tile0, 1))
+        break;
+      for (int i = 0; i < nt && ok; ++i) {
+        const uint32_t tile = tile0 + i;
+        const int st = tile % kQStages, db = tile & 1;
+        const bool more = i + 1 < nt;
+        // S^T / dP^T of the same half of the next tile go in as soon as this
+        // half's softmax has read its buffer (before this half's dV / dK),
+        // if the next tile's Q / dO have landed; otherwise after this dQ
+        bool deferred = !more;
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!deferred) {
+            if (!mbar_wait_warp(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) {
+              ok = false;
+              break;
+            }
+            if (hf == 0)  // one verdict for the warp
+              deferred = __shfl_sync(0xffffffffu,
+                                     mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
+                                                   ((tile + 1) / kQStages) & 1) ? 0 : 1,
+                                     0) != 0;
+            if (!deferred && !issue_sdp(tile + 1, hf)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!mbar_wait_warp(&sm.pds_full[hf], npds[hf] & 1, g)) {
+            ok = false;
+            break;
+          }
+          ++npds[hf];
+          tc_fence_after();
+          const uint32_t ap = tmem + kColPT + 32 * hf;  // P^T of this half (TMEM)
+          const uint64_t as = dSk0 + db * kDsStep + hf * (kTileBytes >> 4);
+          const uint64_t bo = dOmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
+          const uint64_t bq = dQmn0 + st * kStageStep + hf * (kHalfBytes >> 4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // 64 q rows of this half, 16 at a time
+            const uint32_t acc = (i > 0 || hf > 0 || k > 0) ? 1u : 0u;
+            umma_ts_warp(tmem + kColDV, ap + 8 * k, bo + 128 * k, idKV, acc);  // +2048 B / 16 rows
+            umma_ss_warp(tmem + kColDK, as + 2 * k, bq + 128 * k, idKV, acc);
+          }
+          umma_commit_warp(&sm.p_free[hf]);
+          if (hf == 1) umma_commit_warp(&sm.q_empty[st]);  // last reader of Q / dO
+        }
+        if (!ok) break;
+        if (!mbar_wait_warp(&sm.dq_empty, (ndq & 1) ^ 1, g)) break;
+        ++ndq;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time (+2048 B)
+          umma_ss_warp(tmem + kColDQ, dSm0 + db * kDsStep + 128 * k, dKmn + 128 * k, idQ, k > 0);
+        umma_commit_warp(&sm.ds_free[db]);
+        umma_commit_warp(&sm.dq_full);
+        if (more && deferred) {
+          if (!mbar_wait_warp(&sm.q_full[(tile + 1) % kQStages], ((tile + 1) / kQStages) & 1, g) ||
+              !issue_sdp(tile + 1, 0) || !issue_sdp(tile + 1, 1)) {
+            ok = false;
+            break;
+          }
+        }
+      }
+      ntile = tile0 + nt;
+      if (!ok) break;
+      umma_commit_warp(&sm.dkv_full);
+      umma_commit_warp(&sm.kv_empty);
     }
+    umma_commit_warp(&sm.drain);
+    if (lane == 0) drain_wait(&sm.drain, 0);
+    __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax
     // warpgroup hf handles half hf (query rows 64 hf .. 64 hf + 63) of every tile

@@ -45,7 +45,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;  // log2 units
 constexpr int kSchedSlots = 4;
-constexpr int kSchedConsumers = 1 + 4;  // the UMMA thread and 4 softmax warps
+constexpr int kSchedConsumers = 1 + 4;  // the UMMA warp and 4 softmax warps
 
 struct __align__(1024) Smem {
   uint8_t q[kTileBytes];
@@ -85,12 +85,13 @@ __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int 
 // Work units are handed out dynamically (longest first, from the device-built
 // list): the producer thread takes the next index with an atomic and
 // publishes it in a small ring; the UMMA thread and the softmax warps read the
-// ring in order. `lanes` = the calling lanes of the warp.
+// ring in order. `lanes` = the calling lanes of the warp (all of them get the
+// same verdict).
 template <class SmemT>
 __device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g, bool arrive,
                                          unsigned lanes) {
   const int s = n % kSchedSlots;
-  if (!mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g)) return -1;
+  if (!__all_sync(lanes, mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g))) return -1;
   const int w = sm.sched_unit[s];
   __syncwarp(lanes);
   if (arrive) mbar_arrive(&sm.sched_empty[s]);
@@ -111,8 +112,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
            const __grid_constant__ CUtensorMap tm_v, Problem p, const int2* __restrict__ items,
            int32_t* __restrict__ meta) {
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~uintptr_t(1023));
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Guard g{&sm.abort, p.err};
 
@@ -207,74 +207,71 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
-    if (lane == 0) {
-      const uint32_t idS = idesc_bf16(kTile, kTile, false, false);
-      const uint32_t idO = idesc_bf16(kTile, kHeadDim, false, true);
-      const uint32_t qa = smem_u32(sm.q);
-      uint32_t nq = 0, nk = 0, ns = 0, np = 0;
-      auto issue_s = [&](int s) {
-        const uint32_t ka = smem_u32(sm.k[s]);
+    // The whole warp runs this loop (uniform control flow and operands); one
+    // elected lane issues each product and commit.
+    const uint32_t idS = idesc_bf16(kTile, kTile, false, false);
+    const uint32_t idO = idesc_bf16(kTile, kHeadDim, false, true);
+    // descriptors built once; a product adds its byte offset / 16
+    const uint64_t dQ = sdesc_sw128(smem_u32(sm.q), 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v[0]), 8192, 1024);
+    constexpr uint64_t kStageStep = kTileBytes >> 4;  // k[1] - k[0], v[1] - v[0]
+    uint32_t nq = 0, nk = 0, ns = 0, np = 0;
+    bool ok = true;
+    // S of the next key tile (K stage released when it completes)
+    auto next_s = [&]() -> bool {
+      const int s = nk % kKStages;
+      if (!mbar_wait_warp(&sm.k_full[s], (nk / kKStages) & 1, g) ||
+          !mbar_wait_warp(&sm.s_empty, (ns & 1) ^ 1, g))
+        return false;
+      ++ns;
+      tc_fence_after();
+      const uint64_t bk = dK0 + s * kStageStep;
 #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          umma_ss(tmem + kColS, sdesc_sw128(qa + 32 * k, 16, 1024),
-                  sdesc_sw128(ka + 32 * k, 16, 1024), idS, k > 0);
-      };
-      auto issue_pv = [&](int s, bool acc) {
-        const uint32_t va = smem_u32(sm.v[s]);
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc_sw128(va + 2048 * k, 8192, 1024),
-                  idO, acc || k > 0);
-      };
-      bool ok = true;
-      // S of the next key tile (K stage released when it completes)
-      auto next_s = [&]() -> bool {
-        const int s = nk % kKStages;
-        if (!mbar_wait(&sm.k_full[s], (nk / kKStages) & 1, g) ||
-            !mbar_wait(&sm.s_empty, (ns & 1) ^ 1, g))
-          return false;
-        ++ns;
-        tc_fence_after();
-        issue_s(s);
-        umma_commit(&sm.s_full);
-        umma_commit(&sm.k_empty[s]);
-        ++nk;
-        return true;
-      };
-      uint32_t nsched = 0;
-      while (ok) {
-        const int w = next_unit(sm, nsched, g, true, 1u);  // lane 0 alone
-        if (w < 0) break;
-        const Unit u = decode(p, items, w);
-        const int n = u.kt1 - u.kt0;
-        if (!mbar_wait(&sm.q_full, nq & 1, g)) break;
-        ++nq;
-        if (!next_s()) break;
-        if (n == 1) umma_commit(&sm.q_empty);
-        for (int jj = 0; jj < n; ++jj) {
-          if (jj + 1 < n) {
-            if (!next_s()) {
-              ok = false;
-              break;
-            }
-            if (jj + 2 == n) umma_commit(&sm.q_empty);
-          }
-          const int sv = np % kVStages;
-          if (!mbar_wait(&sm.p_full, np & 1, g) ||
-              !mbar_wait(&sm.v_full[sv], (np / kVStages) & 1, g)) {
+      for (int k = 0; k < kHeadDim / 16; ++k)  // +32 bytes per 16 features
+        umma_ss_warp(tmem + kColS, dQ + 2 * k, bk + 2 * k, idS, k > 0);
+      umma_commit_warp(&sm.s_full);
+      umma_commit_warp(&sm.k_empty[s]);
+      ++nk;
+      return true;
+    };
+    uint32_t nsched = 0;
+    while (ok) {
+      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
+      if (w < 0) break;
+      const Unit u = decode(p, items, w);
+      const int n = u.kt1 - u.kt0;
+      if (!mbar_wait_warp(&sm.q_full, nq & 1, g)) break;
+      ++nq;
+      if (!next_s()) break;
+      if (n == 1) umma_commit_warp(&sm.q_empty);
+      for (int jj = 0; jj < n; ++jj) {
+        if (jj + 1 < n) {
+          if (!next_s()) {
             ok = false;
             break;
           }
-          ++np;
-          tc_fence_after();
-          issue_pv(sv, jj > 0);
-          umma_commit(&sm.v_empty[sv]);
-          umma_commit(&sm.o_done);
+          if (jj + 2 == n) umma_commit_warp(&sm.q_empty);
         }
+        const int sv = np % kVStages;
+        if (!mbar_wait_warp(&sm.p_full, np & 1, g) ||
+            !mbar_wait_warp(&sm.v_full[sv], (np / kVStages) & 1, g)) {
+          ok = false;
+          break;
+        }
+        ++np;
+        tc_fence_after();
+        const uint64_t bv = dV0 + sv * kStageStep;
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)  // P from tensor memory; +2048 B of V per 16 keys
+          umma_ts_warp(tmem + kColO, tmem + kColP + 8 * k, bv + 128 * k, idO, (jj > 0 || k > 0) ? 1u : 0u);
+        umma_commit_warp(&sm.v_empty[sv]);
+        umma_commit_warp(&sm.o_done);
       }
-      umma_commit(&sm.drain);  // every product issued above has completed
-      drain_wait(&sm.drain, 0);
     }
+    umma_commit_warp(&sm.drain);  // every product issued above has completed
+    if (lane == 0) drain_wait(&sm.drain, 0);
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;

@@ -28,6 +28,16 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// Bytes to skip from the start of dynamic shared memory to the next 1024-byte
+// boundary (what 128-byte-swizzled tiles need). Offsetting the shared pointer
+// itself, rather than rounding it as an integer, keeps it visibly in the
+// shared window, so its accesses compile to shared loads / stores instead of
+// slower generic ones.
+__device__ __forceinline__ uint32_t align1024_pad(const void* smem) {
+  const uint32_t a = smem_u32(smem);
+  return ((a + 1023u) & ~1023u) - a;
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -100,6 +110,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
       return false;
     }
   }
+}
+
+// mbar_wait by every lane of a converged warp, with one verdict for all of
+// them (so the warp never splits on a timeout).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Guard& g) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, g));
 }
 
 // ------------------------------------------------------------------ TMA
@@ -302,6 +318,42 @@ __device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a, uint64_t b, uint
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
       "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective forms: every lane of a converged warp executes the call
+// with identical operands and one elected lane (the lowest, so always the
+// same one) issues the instruction. Keeping the issuing warp's control flow
+// uniform lets the operands stay warp-uniform, which issues products back to
+// back far faster than a single thread inside a lane branch.
+__device__ __forceinline__ void umma_ss_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_warp(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          smem_u32(bar))
       : "memory");
 }
 
