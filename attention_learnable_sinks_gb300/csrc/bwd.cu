@@ -47,6 +47,7 @@
 // 32-column halves). Q / dO are triple-buffered.
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "sm100.cuh"
@@ -254,7 +255,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (w >= nwork) w = -1;
       {
         const int s = nsched % kSchedSlots;
-        if (!mbar_wait(&sm.sched_empty[s], ((nsched / kSchedSlots) & 1) ^ 1, g)) break;
+        if (!mbar_wait_warp(&sm.sched_empty[s], ((nsched / kSchedSlots) & 1) ^ 1, g)) break;
         if (lane == 0) {
           sm.sched_unit[s] = w;
           mbar_arrive(&sm.sched_full[s]);
@@ -263,7 +264,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
       if (w < 0) break;
       const Unit u = decode(p, items, w);
-      if (!mbar_wait(&sm.kv_empty, (nunit & 1) ^ 1, g)) break;
+      if (!mbar_wait_warp(&sm.kv_empty, (nunit & 1) ^ 1, g)) break;
       if (lane == 0) {
         mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
         tma_load_3d(sm.k, &tm_k, &sm.kv_full, 0, u.kvh, u.base + u.c0);
@@ -284,7 +285,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           dv[e] = q < u.L ? __ldg(bp.D + off) : 0.f;
         }
         const float sink2 = p.sinks ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
-        if (!mbar_wait(&sm.q_empty[st], ((ntile / kQStages) & 1) ^ 1, g)) {
+        if (!mbar_wait_warp(&sm.q_empty[st], ((ntile / kQStages) & 1) ^ 1, g)) {
           ok = false;
           break;
         }
@@ -435,13 +436,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax
-    // warpgroup hf handles half hf (query rows 64 hf .. 64 hf + 63) of every tile
+    // Warpgroup hf handles half hf (query columns 64 hf .. 64 hf + 63) of
+    // every tile, each warp its 32 key rows (TMEM lanes), read as two 16-lane
+    // groups in the .16x256b layout: thread t holds key rows t/4 and t/4 + 8 of
+    // a group and, in every 8-column block, the query pair 2(t%4), 2(t%4) + 1.
+    // A thread so needs the per-query constants of 16 columns, not 64.
     const int hf = (warp - 4) / 4;
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + kColS + 64 * hf;
-    const uint32_t tdP = tmem + lane_off + kColDP + 64 * hf;
+    const int gq = lane >> 2, qq = lane & 3;
     const uint64_t sl2x2 = f2pack(p.scale_log2, p.scale_log2);
     uint32_t nunit = 0, ntile = 0, nsd = 0, nsched = 0;
     bool ok = true;
@@ -449,89 +451,130 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
       if (w < 0) break;
       const Unit u = decode(p, items, w);
-      const int j = u.c0 + r;  // local key index
-      const bool jvalid = r < u.nkeys;
-      const int qlo = p.causal ? j : 0;
-      const int qhi = p.window > 0 ? j + p.window : 0x7fffffff;
+      // this thread's key rows: 32 quarter + 16 grp + 8 rh + gq, grp, rh in {0, 1}
+      const int row_lo = 32 * quarter + gq, row_hi = row_lo + 24;
+      const bool rows_valid = row_hi < u.nkeys;
+      const int qlo_max = p.causal ? u.c0 + row_hi : 0;
+      const int qhi_min = p.window > 0 ? u.c0 + row_lo + p.window : 0x7fffffff;
       uint64_t sa0 = f2pack(0.f, 0.f), sa1 = f2pack(0.f, 0.f);
       for (int i = 0; i < G * u.nq && ok; ++i, ++ntile) {
         const int hh = i / u.nq;
         const int qb = (u.qt0 + i % u.nq) * kTile + 64 * hf;
         const int st = ntile % kQStages, db = ntile & 1;
         // the producer's LSE / D / p_sink rows of this tile (acquire)
-        if (!mbar_wait(&sm.q_full[st], (ntile / kQStages) & 1, g) ||
-            !mbar_wait(&sm.sdp_full[hf], nsd & 1, g)) {
+        if (!mbar_wait_warp(&sm.q_full[st], (ntile / kQStages) & 1, g) ||
+            !mbar_wait_warp(&sm.sdp_full[hf], nsd & 1, g)) {
           ok = false;
           break;
         }
         ++nsd;
         tc_fence_after();
-        const bool full = jvalid && qb >= qlo && qb + 63 < qhi;
-        const int cl = qlo - qb, ch = qhi - qb;
-        const uint32_t tPT = tmem + lane_off + kColPT + 32 * hf;
-        uint8_t* srow = sm.dst[db] + hf * kTileBytes;
-        // 16 query columns at a time; the TMEM load of chunk c+1 is in flight
-        // while chunk c is computed
-        const float4* ld = &sm.rowld[st][32 * hf];
-        const float2* pp = &sm.rowps[st][32 * hf];
-        uint32_t sv[2][16], pv[2][16];
-        tmem_ld16x2_async(tS, tdP, sv[0], pv[0]);
-        tmem_ld_wait();
-        reg_fence16(sv[0]);
-        reg_fence16(pv[0]);
+        // one verdict per warp: both instantiations below are full of
+        // warp-collective instructions, so the warp must not split between them
+        const bool full =
+            __all_sync(0xffffffffu, rows_valid && qb >= qlo_max && qb + 63 < qhi_min);
+        const uint32_t srow = smem_u32(sm.dst[db] + hf * kTileBytes);
+        const float4* ld = &sm.rowld[st][32 * hf + qq];  // + 4 k: {-LSE*log2e x2, -D x2}
+        const float2* pp = &sm.rowps[st][32 * hf + qq];  // + 4 k: p_sink x2
+        // chunk c: lane group c & 1, 8-column blocks kb .. kb + 3 (kb = 4 (c >> 1));
+        // the TMEM loads of chunk c + 1 are in flight while chunk c is computed
+        auto taddr = [&](int c, uint32_t col) {
+          return tmem + ((uint32_t)(32 * quarter + 16 * (c & 1)) << 16) + col + 32 * (c >> 1);
+        };
+        // the masked variant is a separate instantiation, so the arithmetic of
+        // tiles strictly inside the band carries no masking work
+        auto chunks = [&](auto mask_tag) {
+          constexpr bool kMask = decltype(mask_tag)::value;
+          uint32_t sv[2][16], pv[2][16];
+          float4 a4[4];
+          float2 b2[4];
+          tmem_ld16x256b_x4x2_async(taddr(0, kColS + 64 * hf), taddr(0, kColDP + 64 * hf), sv[0], pv[0]);
+          tmem_ld_wait();
+          reg_fence16(sv[0]);
+          reg_fence16(pv[0]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int cur = c & 1;
-          if (c < 3) tmem_ld16x2_async(tS + 16 * (c + 1), tdP + 16 * (c + 1), sv[cur ^ 1], pv[cur ^ 1]);
-          uint32_t pP[8], pS[8];
+          for (int c = 0; c < 4; ++c) {
+            const int cur = c & 1, grp = c & 1, kb = 4 * (c >> 1);
+            if (c < 3)
+              tmem_ld16x256b_x4x2_async(taddr(c + 1, kColS + 64 * hf), taddr(c + 1, kColDP + 64 * hf),
+                                        sv[cur ^ 1], pv[cur ^ 1]);
+            if (grp == 0) {
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const int col = 16 * c + e;
-            const float4 a = ld[col / 2];  // {-LSE*log2e x2, -D x2}
-            const float2 b = pp[col / 2];  // p_sink x2
-            const float2 x = f2unpack(ffma2(f2pack(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])),
-                                            sl2x2, f2pack(a.x, a.y)));
-            float P0 = ex2(x.x), P1 = ex2(x.y);
-            if (!full) {
-              if (!jvalid || col < cl || col >= ch) P0 = 0.f;
-              if (!jvalid || col + 1 < cl || col + 1 >= ch) P1 = 0.f;
+              for (int k = 0; k < 4; ++k) {
+                a4[k] = ld[4 * (kb + k)];
+                b2[k] = pp[4 * (kb + k)];
+              }
             }
-            const uint64_t P = f2pack(P0, P1);
-            const uint64_t t = fmul2(P, f2pack(__uint_as_float(pv[cur][e]), __uint_as_float(pv[cur][e + 1])));
-            if (e & 2)
-              sa1 = ffma2(f2pack(b.x, b.y), t, sa1);
-            else
-              sa0 = ffma2(f2pack(b.x, b.y), t, sa0);
-            const float2 ds = f2unpack(ffma2(P, f2pack(a.z, a.w), t));  // P (dP - D)
-            pP[e / 2] = pack_bf16(P0, P1);
-            pS[e / 2] = pack_bf16(ds.x, ds.y);
-          }
-          if (c == 0) {
-            // P^T half free (dV / dK of the previous tile done), and this
-            // tile's dS^T buffer free (dQ of the tile before that done)
-            if (!mbar_wait(&sm.p_free[hf], (ntile & 1) ^ 1, g) ||
-                !mbar_wait(&sm.ds_free[db], ((ntile >> 1) & 1) ^ 1, g))
-              ok = false;
-          }
-          // P^T (bf16 pairs) to tensor memory -- warp-wide, so always issued;
-          // dS^T to shared memory
-          tmem_st8(tPT + 8 * c, pP);
-          if (ok) {
+            uint32_t pP[8], pS[8];  // [2 k + rh]: block kb + k, key row rh
+            // allowed query columns [clo, chi) of this thread's two key rows
+            // (an empty range for rows past the end of the sequence)
+            int clo[2], chi[2];
 #pragma unroll
-            for (int x = 0; x < 2; ++x)
-              *reinterpret_cast<uint4*>(srow + sw128_offset(r, 2 * c + x)) =
-                  make_uint4(pS[4 * x], pS[4 * x + 1], pS[4 * x + 2], pS[4 * x + 3]);
-          }
-          if (c < 3) {
-            tmem_ld_wait();
-            reg_fence16(sv[cur ^ 1]);
-            reg_fence16(pv[cur ^ 1]);
-            if (c == 2) {  // all of this half's S^T / dP^T is in registers
-              tc_fence_before();
-              mbar_arrive(&sm.sdp_empty[hf]);
+            for (int rh = 0; rh < 2; ++rh) {
+              const int rr = 32 * quarter + 16 * grp + 8 * rh + gq;
+              const int j = u.c0 + rr;
+              clo[rh] = rr < u.nkeys ? (p.causal ? j : 0) - qb : 0x7fffffff;
+              chi[rh] = p.window > 0 ? j + p.window - qb : 0x7fffffff;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+              for (int rh = 0; rh < 2; ++rh) {
+                const int e = 4 * k + 2 * rh;
+                const float2 x = f2unpack(ffma2(f2pack(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])),
+                                                sl2x2, f2pack(a4[k].x, a4[k].y)));
+                float P0 = ex2(x.x), P1 = ex2(x.y);
+                if (kMask) {
+                  const int col = 8 * (kb + k) + 2 * qq;
+                  if (col < clo[rh] || col >= chi[rh]) P0 = 0.f;
+                  if (col + 1 < clo[rh] || col + 1 >= chi[rh]) P1 = 0.f;
+                }
+                const uint64_t P = f2pack(P0, P1);
+                const uint64_t t = fmul2(P, f2pack(__uint_as_float(pv[cur][e]), __uint_as_float(pv[cur][e + 1])));
+                if (rh)
+                  sa1 = ffma2(f2pack(b2[k].x, b2[k].y), t, sa1);
+                else
+                  sa0 = ffma2(f2pack(b2[k].x, b2[k].y), t, sa0);
+                const float2 ds = f2unpack(ffma2(P, f2pack(a4[k].z, a4[k].w), t));  // P (dP - D)
+                pP[2 * k + rh] = pack_bf16(P0, P1);
+                pS[2 * k + rh] = pack_bf16(ds.x, ds.y);
+              }
+            }
+            if (c == 0) {
+              // P^T half free (dV / dK of the previous tile done), and this
+              // tile's dS^T buffer free (dQ of the tile before that done)
+              if (!mbar_wait_warp(&sm.p_free[hf], (ntile & 1) ^ 1, g) ||
+                  !mbar_wait_warp(&sm.ds_free[db], ((ntile >> 1) & 1) ^ 1, g))
+                ok = false;
+            }
+            // P^T (bf16 pairs) to tensor memory -- warp-wide, so always issued:
+            // column 4 (kb + k) + qq of lanes rh = 0 / 1
+            tmem_st16x128b_x4(tmem + ((uint32_t)(32 * quarter + 16 * grp) << 16) + kColPT + 32 * hf + 4 * kb, pP);
+            // dS^T to shared memory, as 8x8 blocks: block kb + k, rows rh
+            if (ok) {
+#pragma unroll
+              for (int s2 = 0; s2 < 2; ++s2) {
+                const int m = lane >> 3, rh = m & 1, k = 2 * s2 + (m >> 1);
+                const uint32_t rj = 32 * quarter + 16 * grp + 8 * rh + (lane & 7);
+                stmatrix_x4(srow + rj * 128u + ((uint32_t)((kb + k) ^ (lane & 7)) << 4), pS[4 * s2],
+                            pS[4 * s2 + 1], pS[4 * s2 + 2], pS[4 * s2 + 3]);
+              }
+            }
+            if (c < 3) {
+              tmem_ld_wait();
+              reg_fence16(sv[cur ^ 1]);
+              reg_fence16(pv[cur ^ 1]);
+              if (c == 2) {  // all of this half's S^T / dP^T is in registers
+                tc_fence_before();
+                mbar_arrive(&sm.sdp_empty[hf]);
+              }
             }
           }
-        }
+        };
+        if (full)
+          chunks(std::false_type{});
+        else
+          chunks(std::true_type{});
         tmem_st_wait();
         if (!ok) break;
         fence_async_smem();
@@ -550,15 +593,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
       }
       if (!ok) break;
-      // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the dK rows
-      if (!mbar_wait(&sm.dkv_full, nunit & 1, g)) break;
+      // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the dK rows,
+      // one key row (TMEM lane) per thread
+      if (!mbar_wait_warp(&sm.dkv_full, nunit & 1, g)) break;
       ++nunit;
       tc_fence_after();
+      const int r = 32 * quarter + lane;
+      const int j = u.c0 + r;
       uint32_t a[64];
-      tmem_ld64(tmem + lane_off + (hf == 0 ? kColDV : kColDK), a);
+      tmem_ld64(tmem + ((uint32_t)(32 * quarter) << 16) + (hf == 0 ? kColDV : kColDK), a);
       tc_fence_before();
       mbar_arrive(&sm.dkv_empty);
-      if (jvalid) {
+      if (r < u.nkeys) {
         const float sc = hf == 0 ? 1.f : p.scale;
         uint32_t ob[32];
 #pragma unroll
@@ -586,7 +632,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int i = 0; i < G * u.nq; ++i) {
         const int h = u.kvh * G + i / u.nq;
         const int q0 = (u.qt0 + i % u.nq) * kTile;
-        if (!mbar_wait(&sm.dq_full, ndq & 1, g)) {
+        if (!mbar_wait_warp(&sm.dq_full, ndq & 1, g)) {
           ok = false;
           break;
         }
@@ -602,7 +648,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             bulk_wait_read0();  // the previous reduce has read the staging buffer
             mbar_arrive(&sm.stg_free);
           }
-          if (!mbar_wait(&sm.stg_free, nstg & 1, g)) {
+          if (!mbar_wait_warp(&sm.stg_free, nstg & 1, g)) {
             ok = false;
             break;
           }

@@ -294,7 +294,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       float l = p.sinks ? 1.f : 0.f;
       for (int jj = 0; jj < n; ++jj) {
         const int c0 = (u.kt0 + jj) * kTile;
-        if (!mbar_wait(&sm.s_full, nsf & 1, g)) {
+        if (!mbar_wait_warp(&sm.s_full, nsf & 1, g)) {
           ok = false;
           break;
         }
@@ -348,7 +348,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         l += sum0 + sum1;
         if (jj > 0) {
           // PV(jj-1) must be complete: it reads P and accumulates into O
-          if (!mbar_wait(&sm.o_done, nod & 1, g)) {
+          if (!mbar_wait_warp(&sm.o_done, nod & 1, g)) {
             ok = false;
             break;
           }
@@ -373,7 +373,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
       if (!ok) break;
       // epilogue: O / l, LSE
-      if (!mbar_wait(&sm.o_done, nod & 1, g)) break;
+      if (!mbar_wait_warp(&sm.o_done, nod & 1, g)) break;
       ++nod;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;

@@ -112,6 +112,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// mbar_wait by lane 0 of a converged warp for all of it: one thread polls,
+// the warp barrier then orders the other lanes after its acquire, and every
+// lane gets the same verdict.
+__device__ __forceinline__ bool mbar_wait_lane0(uint64_t* bar, uint32_t parity, const Guard& g) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, g) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 // mbar_wait by every lane of a converged warp, with one verdict for all of
 // them (so the warp never splits on a timeout).
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Guard& g) {
@@ -244,6 +255,37 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 __device__ __forceinline__ void reg_fence16(uint32_t (&a)[16]) {
   asm volatile("" : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]) : : "memory");
+}
+
+// Two .16x256b loads of four repetitions each (16 registers), no wait. The
+// 16 TMEM lanes at the address are split over the warp: in 8-column block i,
+// thread t holds lanes t/4 and t/4 + 8, columns 2(t%4) and 2(t%4) + 1:
+// r[4i..4i+3] = (t/4, 2(t%4)), (t/4, 2(t%4)+1), (t/4+8, 2(t%4)), (t/4+8, 2(t%4)+1).
+__device__ __forceinline__ void tmem_ld16x256b_x4x2_async(uint32_t ta, uint32_t tb, uint32_t (&a)[16],
+                                                         uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// .16x128b store of four repetitions (no wait): in 4-column block i, thread t
+// writes r[2i] to (lane t/4, column t%4) and r[2i+1] to (lane t/4 + 8, same column).
+__device__ __forceinline__ void tmem_st16x128b_x4(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// Four 8x8 matrices of 16-bit elements to shared memory (warp-collective):
+// register m of thread t is row t/4, elements 2(t%4) and 2(t%4)+1 (low half
+// first) of matrix m; lane l gives the address of row l%8 of matrix l/8.
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
 }
 
 // Store 32 consecutive 32-bit columns of this thread's lane (no wait).
