@@ -319,7 +319,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ------------------------------------------------------------ UMMA issuer
     // The whole warp runs this loop (uniform control flow and operands); one
     // elected lane issues each product and commit.
-    const uint32_t idS = idesc_bf16(kTile, 64, false, false);
+    const uint32_t idS = idesc_bf16(kTile, kTile, false, false);
     const uint32_t idKV = idesc_bf16(kTile, kHeadDim, false, true);
     const uint32_t idQ = idesc_bf16(kTile, kHeadDim, true, true);
     // descriptors built once; a product adds its byte offset / 16
@@ -335,22 +335,26 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint64_t dSm0 = sdesc_sw128(smem_u32(sm.dst[0]), kTileBytes, 1024);
     constexpr uint64_t kStageStep = kTileBytes >> 4;        // q[1] - q[0], dout[1] - dout[0]
     constexpr uint64_t kDsStep = (2 * kTileBytes) >> 4;     // dst[1] - dst[0]
-    uint32_t nunit = 0, ntile = 0, nsdp[2] = {0, 0}, npds[2] = {0, 0}, ndq = 0;
+    uint32_t nunit = 0, ntile = 0, nsdp = 0, npds[2] = {0, 0}, ndq = 0;
     bool ok = true;
-    // S^T and dP^T of half hf of a query tile (its Q / dO stage must be full)
-    auto issue_sdp = [&](uint32_t tile, int hf) -> bool {
+    // S^T and dP^T of a whole query tile, N = 128 (its Q / dO stage must be
+    // full, and both softmax warpgroups must have read the previous tile's)
+    auto issue_sdp = [&](uint32_t tile) -> bool {
       const int st = tile % kQStages;
-      if (!mbar_wait_warp(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) return false;
-      ++nsdp[hf];
+      if (!mbar_wait_warp(&sm.sdp_empty[0], (nsdp & 1) ^ 1, g) ||
+          !mbar_wait_warp(&sm.sdp_empty[1], (nsdp & 1) ^ 1, g))
+        return false;
+      ++nsdp;
       tc_fence_after();
-      const uint64_t bq = dQk0 + st * kStageStep + hf * (kHalfBytes >> 4);
-      const uint64_t bo = dOk0 + st * kStageStep + hf * (kHalfBytes >> 4);
+      const uint64_t bq = dQk0 + st * kStageStep;
+      const uint64_t bo = dOk0 + st * kStageStep;
 #pragma unroll
       for (int k = 0; k < kHeadDim / 16; ++k) {  // +32 bytes per 16 features
-        umma_ss_warp(tmem + kColS + 64 * hf, dK + 2 * k, bq + 2 * k, idS, k > 0);
-        umma_ss_warp(tmem + kColDP + 64 * hf, dV + 2 * k, bo + 2 * k, idS, k > 0);
+        umma_ss_warp(tmem + kColS, dK + 2 * k, bq + 2 * k, idS, k > 0);
+        umma_ss_warp(tmem + kColDP, dV + 2 * k, bo + 2 * k, idS, k > 0);
       }
-      umma_commit_warp(&sm.sdp_full[hf]);
+      umma_commit_warp(&sm.sdp_full[0]);
+      umma_commit_warp(&sm.sdp_full[1]);
       return true;
     };
     uint32_t nsched = 0;
@@ -364,32 +368,32 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       ++nunit;
       const uint32_t tile0 = ntile;
       if (!mbar_wait_warp(&sm.q_full[tile0 % kQStages], (tile0 / kQStages) & 1, g) ||
-          !issue_sdp(tile0, 0) || !issue_sdp(tile0, 1))
+          !issue_sdp(tile0))
         break;
       for (int i = 0; i < nt && ok; ++i) {
         const uint32_t tile = tile0 + i;
         const int st = tile % kQStages, db = tile & 1;
         const bool more = i + 1 < nt;
-        // S^T / dP^T of the same half of the next tile go in as soon as this
-        // half's softmax has read its buffer (before this half's dV / dK),
-        // if the next tile's Q / dO have landed; otherwise after this dQ
+        // S^T / dP^T of the next tile go in as soon as both softmax
+        // warpgroups have read this tile's (before this tile's dV / dK), if
+        // the next tile's Q / dO have landed; otherwise after this dQ
         bool deferred = !more;
-        for (int hf = 0; hf < 2; ++hf) {
-          if (!deferred) {
-            if (!mbar_wait_warp(&sm.sdp_empty[hf], (nsdp[hf] & 1) ^ 1, g)) {
-              ok = false;
-              break;
-            }
-            if (hf == 0)  // one verdict for the warp
-              deferred = __shfl_sync(0xffffffffu,
-                                     mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
-                                                   ((tile + 1) / kQStages) & 1) ? 0 : 1,
-                                     0) != 0;
-            if (!deferred && !issue_sdp(tile + 1, hf)) {
-              ok = false;
-              break;
-            }
+        if (!deferred) {
+          if (!mbar_wait_warp(&sm.sdp_empty[0], (nsdp & 1) ^ 1, g) ||
+              !mbar_wait_warp(&sm.sdp_empty[1], (nsdp & 1) ^ 1, g)) {
+            ok = false;
+            break;
           }
+          deferred = __shfl_sync(0xffffffffu,
+                                 mbar_try_wait(&sm.q_full[(tile + 1) % kQStages],
+                                               ((tile + 1) / kQStages) & 1) ? 0 : 1,
+                                 0) != 0;
+          if (!deferred && !issue_sdp(tile + 1)) {
+            ok = false;
+            break;
+          }
+        }
+        for (int hf = 0; hf < 2; ++hf) {
           if (!mbar_wait_warp(&sm.pds_full[hf], npds[hf] & 1, g)) {
             ok = false;
             break;
@@ -410,7 +414,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           if (hf == 1) umma_commit_warp(&sm.q_empty[st]);  // last reader of Q / dO
         }
         if (!ok) break;
-        if (!mbar_wait_warp(&sm.dq_empty, (ndq & 1) ^ 1, g)) break;
+        if (!mbar_wait_warp(&sm.dq_empty, (ndq & 1) ^ 1, g)) {
+          ok = false;
+          break;
+        }
         ++ndq;
         tc_fence_after();
 #pragma unroll
@@ -420,7 +427,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         umma_commit_warp(&sm.dq_full);
         if (more && deferred) {
           if (!mbar_wait_warp(&sm.q_full[(tile + 1) % kQStages], ((tile + 1) / kQStages) & 1, g) ||
-              !issue_sdp(tile + 1, 0) || !issue_sdp(tile + 1, 1)) {
+              !issue_sdp(tile + 1)) {
             ok = false;
             break;
           }

@@ -69,6 +69,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase (try_wait may hold the thread for a while
+// when the phase is not yet complete; this returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared abort state of a CTA plus the device error word.
 struct Guard {
   volatile int* abort;  // in shared memory
@@ -121,6 +135,27 @@ __device__ __forceinline__ bool mbar_wait_lane0(uint64_t* bar, uint32_t parity, 
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
+}
+
+// As mbar_wait, but polling without sleeping (for waits on the critical path
+// that usually end within a few hundred cycles).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const Guard& g) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0) {
+      if (g.aborted()) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        g.fail(kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_spin_warp(uint64_t* bar, uint32_t parity, const Guard& g) {
+  return __all_sync(0xffffffffu, mbar_wait_spin(bar, parity, g));
 }
 
 // mbar_wait by every lane of a converged warp, with one verdict for all of
