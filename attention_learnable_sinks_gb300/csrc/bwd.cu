@@ -17,7 +17,7 @@
 //               the fp32 dq accumulator
 //   main        key-stationary, on tcgen05 tensor cores (below)
 //   finish      dq = bf16(dq accumulator); dS_h = -(fixed-order fp64 sum of
-//               the partials)
+//               the partials, one warp per head)
 //
 // Main kernel. One CTA per SM owns a 128-key tile of one kv head at a time
 // (persistent; units are taken dynamically from the device-built key-tile
@@ -695,16 +695,20 @@ constexpr int kFinishThreads = 256;
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
   const Problem& p = bp.f;
-  if (blockIdx.x == 0 && bp.dsinks) {
-    for (int h = threadIdx.x; h < p.Hq; h += kFinishThreads) {
-      double acc = 0.0;
-      if (p.sinks) {
-        const int n = kmeta[0];
-        const float* part = bp.sink_part + (int64_t)h * bp.part_stride * 8;
-        for (int c = 0; c < 8 * n; ++c) acc += (double)part[c];
-      }
-      bp.dsinks[h] = (float)(-acc);
+  // dS_h: one warp per head. Lane-strided fp64 sums, then a fixed butterfly,
+  // so the result does not depend on timing.
+  const int hw = blockIdx.x * (kFinishThreads / 32) + threadIdx.x / 32;
+  if (bp.dsinks && hw < p.Hq) {
+    const int lane = threadIdx.x & 31;
+    double acc = 0.0;
+    if (p.sinks) {
+      const int n = 8 * kmeta[0];
+      const float* part = bp.sink_part + (int64_t)hw * bp.part_stride * 8;
+      for (int c = lane; c < n; c += 32) acc += (double)part[c];
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) bp.dsinks[hw] = (float)(-acc);
   }
   const int64_t n8 = (int64_t)p.total * p.Hq * kHeadDim / 8;
   const int64_t e = (int64_t)blockIdx.x * kFinishThreads + threadIdx.x;  // 8 elements each
@@ -756,7 +760,8 @@ cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int n
                               cudaStream_t s) {
   (void)num_sms;
   const int64_t n8 = (int64_t)p.f.total * p.f.Hq * kHeadDim / 8;
-  const int64_t blocks = std::max<int64_t>(1, (n8 + kFinishThreads - 1) / kFinishThreads);
+  const int64_t head_blocks = (p.f.Hq + kFinishThreads / 32 - 1) / (kFinishThreads / 32);
+  const int64_t blocks = std::max<int64_t>(head_blocks, (n8 + kFinishThreads - 1) / kFinishThreads);
   finish_kernel<<<(unsigned)blocks, kFinishThreads, 0, s>>>(p, ktiles.meta);
   note_launch();
   return cudaGetLastError();
