@@ -41,6 +41,7 @@ class BwdParams(ctypes.Structure):
         ("dsinks", _c_void_p),
         ("workspace", _c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("timing_events", _c_void_p * 2),
+        ("accumulate_dsinks", ctypes.c_int32),
     ]
 
 

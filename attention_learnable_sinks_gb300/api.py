@@ -92,9 +92,10 @@ def forward(q, k, v, sinks, cu_seqlens, max_seqlen, *, causal=True, window=0, sc
 
 def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=True, window=0,
              scale=None, dq=None, dk=None, dv=None, dsinks=None, workspace=None,
-             timing_events=None):
+             timing_events=None, accumulate_dsinks=False):
     """dq, dk, dv (bf16, shaped like q, k, v but contiguous) and dsinks [Hq]
-    fp32 (None when ``sinks`` is None)."""
+    fp32 (None when ``sinks`` is None). With ``accumulate_dsinks`` the sink
+    gradient is added to the given ``dsinks`` instead of overwriting it."""
     _validate_inputs(q, k, v, sinks, cu_seqlens)
     for name, t in (("o", o), ("dout", dout)):
         _check_tokens(name, t, 1)
@@ -118,6 +119,9 @@ def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=Tru
     p.dsinks = _ptr(dsinks)
     p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
     p.timing_events[0], p.timing_events[1] = _events(timing_events)
+    if accumulate_dsinks and dsinks is None:
+        raise ValueError("accumulate_dsinks needs a dsinks tensor to add to")
+    p.accumulate_dsinks = 1 if accumulate_dsinks else 0
     check(L.sinkattn_bwd(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_bwd")
     return dq, dk, dv, dsinks
 
@@ -170,3 +174,136 @@ def sink_attention(q, k, v, sinks=None, cu_seqlens=None, max_seqlen=None, *, cau
         max_seqlen = int(lens.max().item()) if lens.numel() else 0
     o = _SinkAttention.apply(q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale)
     return o.reshape(B, T, *o.shape[1:]) if batched else o
+
+
+def _split_sequences(lens, causal: bool, window: int, groups: int):
+    """Boundaries (sequence indices) of up to ``groups`` runs of consecutive
+    sequences with about equal attention cost (allowed pairs)."""
+    def cost(L):
+        if not causal:
+            return L * L
+        if window > 0 and window < L:
+            return window * (window + 1) // 2 + (L - window) * window
+        return L * (L + 1) // 2
+    costs = [cost(int(L)) for L in lens]
+    total = sum(costs)
+    groups = max(1, min(groups, len(costs)))
+    bounds, acc, g = [0], 0, 1
+    for i, c in enumerate(costs):
+        acc += c
+        if g < groups and acc >= total * g / groups and i + 1 < len(costs):
+            bounds.append(i + 1)
+            g += 1
+    bounds.append(len(costs))
+    return bounds
+
+
+class HostPipeline:
+    """Forward + backward of a packed batch held in pinned host memory.
+
+    The batch is split into groups of whole sequences. The host-to-device
+    copies of one group, the kernels of another and the device-to-host copies
+    of a third run at the same time on three streams; the sink gradient is
+    accumulated over the groups by the backward itself. Results equal one
+    ``forward`` + ``backward`` over the whole batch (dS_h up to the order of
+    its float additions). Device buffers, workspaces and streams are made
+    once, for one batch shape (``cu_seqlens``, heads).
+    """
+
+    def __init__(self, cu_seqlens, Hq: int, Hkv: int, *, causal=True, window=0, scale=None,
+                 groups: int = 2, device=None):
+        device = torch.device(device if device is not None else "cuda")
+        cu = [int(x) for x in cu_seqlens.tolist()]
+        lens = [b - a for a, b in zip(cu[:-1], cu[1:])]
+        self.bounds = _split_sequences(lens, causal, window, groups)
+        self.causal, self.window, self.scale = causal, window, scale
+        self.Hq, self.Hkv, self.total = Hq, Hkv, cu[-1]
+        self.device = device
+        d = HEAD_DIM
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.q = torch.empty(self.total, Hq, d, **bf)
+        self.k = torch.empty(self.total, Hkv, d, **bf)
+        self.v = torch.empty(self.total, Hkv, d, **bf)
+        self.dout = torch.empty(self.total, Hq, d, **bf)
+        self.o = torch.empty_like(self.q)
+        self.dq = torch.empty_like(self.q)
+        self.dk = torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.v)
+        self.sinks = torch.empty(Hq, dtype=torch.float32, device=device)
+        self.dsinks = torch.empty(Hq, dtype=torch.float32, device=device)
+        self.groups = []
+        fw = bw = 1
+        for a, b in zip(self.bounds[:-1], self.bounds[1:]):
+            t0, t1 = cu[a], cu[b]
+            local = torch.tensor([x - t0 for x in cu[a:b + 1]], dtype=torch.int32)
+            self.groups.append({
+                "t0": t0, "t1": t1, "nseq": b - a, "max_seqlen": max(lens[a:b]) if b > a else 0,
+                "cu_host": local.pin_memory(),
+                "cu": torch.empty(b - a + 1, dtype=torch.int32, device=device),
+                "lse": torch.empty(Hq, t1 - t0, dtype=torch.float32, device=device),
+                "qkv": torch.cuda.Event(), "do": torch.cuda.Event(),
+                "fwd": torch.cuda.Event(), "bwd": torch.cuda.Event(),
+            })
+            fw = max(fw, workspace_bytes("fwd", b - a, t1 - t0, Hq, Hkv))
+            bw = max(bw, workspace_bytes("bwd", b - a, t1 - t0, Hq, Hkv))
+        self.ws_f = torch.empty(fw, dtype=torch.uint8, device=device)
+        self.ws_b = torch.empty(bw, dtype=torch.uint8, device=device)
+        self.s_in = torch.cuda.Stream(device)
+        self.s_run = torch.cuda.Stream(device)
+        self.s_out = torch.cuda.Stream(device)
+
+    def h2d_bytes(self) -> int:
+        per_tok = (2 * self.Hq + 2 * self.Hkv) * HEAD_DIM * 2
+        return self.total * per_tok + 4 * self.Hq + sum(4 * g["cu"].numel() for g in self.groups)
+
+    def d2h_bytes(self) -> int:
+        return self.total * (2 * self.Hq + 2 * self.Hkv) * HEAD_DIM * 2 + 4 * self.Hq
+
+    def run(self, hq, hk, hv, hdout, hsinks, ho, hdq, hdk, hdv, hdsinks):
+        """Enqueue the whole batch: host inputs (pinned, shaped like the device
+        buffers) in, host outputs out. Ordered after the current stream's work;
+        the current stream waits for the last copy, so synchronising it (or an
+        event recorded on it) covers everything."""
+        cur = torch.cuda.current_stream(self.device)
+        # inputs: a group's q / k / v first (the forward needs only them), then dO
+        self.s_in.wait_stream(cur)
+        with torch.cuda.stream(self.s_in):
+            self.sinks.copy_(hsinks, non_blocking=True)
+            for g in self.groups:
+                sl = slice(g["t0"], g["t1"])
+                g["cu"].copy_(g["cu_host"], non_blocking=True)
+                for dst, src in ((self.q, hq), (self.k, hk), (self.v, hv)):
+                    dst[sl].copy_(src[sl], non_blocking=True)
+                g["qkv"].record(self.s_in)
+                self.dout[sl].copy_(hdout[sl], non_blocking=True)
+                g["do"].record(self.s_in)
+        self.s_run.wait_stream(cur)
+        with torch.cuda.stream(self.s_run):
+            for i, g in enumerate(self.groups):
+                sl = slice(g["t0"], g["t1"])
+                q, k, v, do = self.q[sl], self.k[sl], self.v[sl], self.dout[sl]
+                o = self.o[sl]
+                self.s_run.wait_event(g["qkv"])
+                forward(q, k, v, self.sinks, g["cu"], g["max_seqlen"], causal=self.causal,
+                        window=self.window, scale=self.scale, out=o, lse=g["lse"],
+                        workspace=self.ws_f)
+                g["fwd"].record(self.s_run)
+                self.s_run.wait_event(g["do"])
+                backward(q, k, v, self.sinks, g["cu"], g["max_seqlen"], o, g["lse"], do,
+                         causal=self.causal, window=self.window, scale=self.scale,
+                         dq=self.dq[sl], dk=self.dk[sl], dv=self.dv[sl], dsinks=self.dsinks,
+                         workspace=self.ws_b, accumulate_dsinks=i > 0)
+                g["bwd"].record(self.s_run)
+        # outputs: a group's o as soon as its forward is done, then its gradients
+        self.s_out.wait_stream(cur)
+        with torch.cuda.stream(self.s_out):
+            for g in self.groups:
+                sl = slice(g["t0"], g["t1"])
+                self.s_out.wait_event(g["fwd"])
+                ho[sl].copy_(self.o[sl], non_blocking=True)
+                self.s_out.wait_event(g["bwd"])
+                for dst, src in ((hdq, self.dq), (hdk, self.dk), (hdv, self.dv)):
+                    dst[sl].copy_(src[sl], non_blocking=True)
+            hdsinks.copy_(self.dsinks, non_blocking=True)
+        cur.wait_stream(self.s_out)
+        return ho, hdq, hdk, hdv, hdsinks

@@ -275,7 +275,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
     return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_bwd_workspace_size()");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (f.total == 0) {
-    if (a->dsinks) {
+    if (a->dsinks && !a->accumulate_dsinks) {
       cudaError_t e = cudaMemsetAsync(a->dsinks, 0, sizeof(float) * f.Hq, s);
       if (e != cudaSuccess) return cuda_fail(e, "dsinks clear");
     }
@@ -290,6 +290,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.dk = static_cast<__nv_bfloat16*>(a->dk);
   bp.dv = static_cast<__nv_bfloat16*>(a->dv);
   bp.dsinks = a->dsinks;
+  bp.accumulate_dsinks = a->accumulate_dsinks != 0;
   bp.D = reinterpret_cast<float*>(ws + l.D);
   bp.sink_part = reinterpret_cast<float*>(ws + l.part);
   bp.dq_acc = reinterpret_cast<float*>(ws + l.dq_acc);

@@ -156,7 +156,7 @@ __device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g,
                                          unsigned lanes) {
   const int s = n % kSchedSlots;
   if (!__all_sync(lanes, mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g))) return -1;
-  const int w = sm.sched_unit[s];
+  const int w = __shfl_sync(lanes, sm.sched_unit[s], 0);  // warp-uniform
   __syncwarp(lanes);
   if (arrive) mbar_arrive(&sm.sched_empty[s]);
   ++n;
@@ -239,7 +239,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
+  // broadcast so the compiler sees a warp-uniform value (UMMA operands)
+  const uint32_t tmem = __shfl_sync(0xffffffffu, sm.tmem_base, 0);
   const int nwork = meta[0] * p.Hkv;
   const int G = p.G;
 
@@ -362,7 +363,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
       if (w < 0) break;
       const Unit u = decode(p, items, w);
-      const int nt = G * u.nq;
+      const int nt = __shfl_sync(0xffffffffu, G * u.nq, 0);  // warp-uniform trip count
       if (!mbar_wait_warp(&sm.kv_full, nunit & 1, g)) break;
       if (!mbar_wait_warp(&sm.dkv_empty, (nunit & 1) ^ 1, g)) break;
       ++nunit;
@@ -708,7 +709,7 @@ finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) bp.dsinks[hw] = (float)(-acc);
+    if (lane == 0) bp.dsinks[hw] = bp.accumulate_dsinks ? bp.dsinks[hw] + (float)(-acc) : (float)(-acc);
   }
   const int64_t n8 = (int64_t)p.total * p.Hq * kHeadDim / 8;
   const int64_t e = (int64_t)blockIdx.x * kFinishThreads + threadIdx.x;  // 8 elements each

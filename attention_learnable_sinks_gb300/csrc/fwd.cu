@@ -92,7 +92,7 @@ __device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g,
                                          unsigned lanes) {
   const int s = n % kSchedSlots;
   if (!__all_sync(lanes, mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g))) return -1;
-  const int w = sm.sched_unit[s];
+  const int w = __shfl_sync(lanes, sm.sched_unit[s], 0);  // warp-uniform
   __syncwarp(lanes);
   if (arrive) mbar_arrive(&sm.sched_empty[s]);
   ++n;
@@ -150,7 +150,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
+  // broadcast so the compiler sees a warp-uniform value (UMMA operands)
+  const uint32_t tmem = __shfl_sync(0xffffffffu, sm.tmem_base, 0);
   const int nwork = meta[0] * p.Hq;
 
   if (warp == 0) {
@@ -240,7 +241,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
       if (w < 0) break;
       const Unit u = decode(p, items, w);
-      const int n = u.kt1 - u.kt0;
+      const int n = __shfl_sync(0xffffffffu, u.kt1 - u.kt0, 0);  // warp-uniform trip count
       if (!mbar_wait_warp(&sm.q_full, nq & 1, g)) break;
       ++nq;
       if (!next_s()) break;
@@ -315,13 +316,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           for (int c = 0; c < kTile; ++c)
             if (c < cl || c >= ch) s[c] = -INFINITY;
         }
+        // row maximum with three-input max (two new values per instruction)
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 4; c < kTile; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 4; c < kTile; c += 8) {
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
         }
         const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
         // lazy rescale: keep the stale maximum unless it grew by > 2^8

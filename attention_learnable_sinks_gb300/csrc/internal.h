@@ -42,6 +42,7 @@ struct BwdProblem {
   float* dq_acc;               // [total, Hq, 64] fp32 workspace
   int32_t nchunks;             // token chunks of the preprocess pass
   int32_t part_stride;         // key-tile capacity
+  int32_t accumulate_dsinks;   // add to dsinks instead of overwriting it
 };
 
 // Tile work list in the workspace: meta[0] = number of items, meta[1] = the

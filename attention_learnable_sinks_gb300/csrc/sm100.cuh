@@ -478,6 +478,19 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// max(a, b, c) in one instruction (sm_100 family)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a 128-byte-swizzled
 // tile of 128-byte rows (the layout TMA writes with 128-byte swizzling).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {

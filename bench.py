@@ -334,30 +334,22 @@ def run_gb300(args):
     ms_per_step = total_ms / K
     value = flops * world * K / (total_ms / 1e3) / 1e12
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: HostPipeline
+    # streams groups of whole sequences, overlapping each group's copies with
+    # another group's kernels
     hq, hk, hv, hdo = (t.pin_memory() for t in (w.q, w.k, w.v, w.dout))
-    hs, hcu = w.sinks.pin_memory(), w.cu_seqlens.pin_memory()
+    hs = w.sinks.pin_memory()
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
     hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
     hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
     hds = torch.empty(ds.shape, dtype=ds.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hs, hcu))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv, hds))
+    pipe = api.HostPipeline(w.cu_seqlens, w.Hq, w.Hkv, causal=w.causal, window=w.window,
+                            scale=w.scale, groups=args.e2e_groups, device=device)
+    h2d, d2h = pipe.h2d_bytes(), pipe.d2h_bytes()
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        s.copy_(hs, non_blocking=True)
-        cu.copy_(hcu, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hdq.copy_(dq, non_blocking=True)
-        hdk.copy_(dk, non_blocking=True)
-        hdv.copy_(dv, non_blocking=True)
-        hds.copy_(ds, non_blocking=True)
+        pipe.run(hq, hk, hv, hdo, hs, ho, hdq, hdk, hdv, hds)
 
     for _ in range(max(1, args.warmup // 2)):
         e2e_step()
@@ -430,6 +422,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="dense",
                     choices=("tiny", "dense", "window", "varlen", "long", "long_window"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=2,
+                    help="groups of whole sequences streamed by the end-to-end leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

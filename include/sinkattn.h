@@ -118,11 +118,15 @@ typedef struct sinkattn_bwd_params {
   void* dq;                    /* out: bf16 [total, Hq, 64]                    */
   void* dk;                    /* out: bf16 [total, Hkv, 64]                   */
   void* dv;                    /* out: bf16 [total, Hkv, 64]                   */
-  float* dsinks;               /* out: fp32 [Hq], overwritten (not accumulated);
-                                  may be NULL; all zero when sinks is NULL    */
+  float* dsinks;               /* out: fp32 [Hq]; may be NULL; the gradient is
+                                  zero when sinks is NULL                     */
   void* workspace;             /* >= sinkattn_bwd_workspace_size() bytes       */
   size_t workspace_bytes;
   void* timing_events[2];      /* optional, around the main backward kernel    */
+  int32_t accumulate_dsinks;   /* 0: dsinks = dL/dS_h; nonzero: dsinks +=
+                                  dL/dS_h (gradient accumulation over several
+                                  calls, e.g. micro-batches or groups of
+                                  sequences of one batch)                     */
 } sinkattn_bwd_params;
 
 /* Workspace sizes in bytes for a problem of this shape (0 on bad input). */

@@ -113,3 +113,16 @@ def test_backward_rejects_missing_outputs():
     b.fwd.lse = None
     assert lib.sinkattn_bwd(ctypes.byref(b), None) == 1
     assert lib.sinkattn_bwd(None, None) == 1
+
+
+def test_sequence_groups_for_the_host_pipeline():
+    from attention_learnable_sinks_gb300.api import _split_sequences
+    # bounds are sequence indices, cover everything, and cut only between sequences
+    assert _split_sequences([2048] * 4, True, 0, 2) == [0, 2, 4]
+    assert _split_sequences([2048] * 4, True, 0, 1) == [0, 4]
+    assert _split_sequences([5], True, 0, 3) == [0, 1]
+    assert _split_sequences([], True, 0, 2) == [0, 0]
+    b = _split_sequences([100, 4000, 50, 50, 3000], True, 0, 3)
+    assert b[0] == 0 and b[-1] == 5 and all(x < y for x, y in zip(b, b[1:]))
+    # a windowed cost grows linearly, so equal lengths still split evenly
+    assert _split_sequences([1000] * 6, True, 128, 3) == [0, 2, 4, 6]
