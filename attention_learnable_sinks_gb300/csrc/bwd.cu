@@ -265,13 +265,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
       if (w < 0) break;
       const Unit u = decode(p, items, w);
-      if (!mbar_wait_warp(&sm.kv_empty, (nunit & 1) ^ 1, g)) break;
-      if (lane == 0) {
-        mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
-        tma_load_3d(sm.k, &tm_k, &sm.kv_full, 0, u.kvh, u.base + u.c0);
-        tma_load_3d(sm.v, &tm_v, &sm.kv_full, 0, u.kvh, u.base + u.c0);
-      }
-      ++nunit;
+      // the unit's K / V load goes out right after its first Q / dO tile: a
+      // Q / dO stage frees up a few tiles before the previous unit's K / V
+      // do, so the two latencies overlap at the unit boundary
+      bool kv_loaded = false;
       for (int i = 0; i < G * u.nq; ++i, ++ntile) {
         const int h = u.kvh * G + i / u.nq;
         const int q0 = (u.qt0 + i % u.nq) * kTile;
@@ -309,7 +306,22 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           tma_load_3d(sm.q[st], &tm_q, &sm.q_full[st], 0, h, u.base + q0);
           tma_load_3d(sm.dout[st], &tm_do, &sm.q_full[st], 0, h, u.base + q0);
         }
+        if (!kv_loaded) {
+          if (!mbar_wait_warp(&sm.kv_empty, (nunit & 1) ^ 1, g)) {
+            ++ntile;  // this tile's copy is in flight: the abort drain must see it
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
+            tma_load_3d(sm.k, &tm_k, &sm.kv_full, 0, u.kvh, u.base + u.c0);
+            tma_load_3d(sm.v, &tm_v, &sm.kv_full, 0, u.kvh, u.base + u.c0);
+          }
+          ++nunit;
+          kv_loaded = true;
+        }
       }
+      if (!ok) break;
     }
     if (lane == 0 && g.aborted()) {
       if (nunit) drain_wait(&sm.kv_full, (nunit - 1) & 1);
