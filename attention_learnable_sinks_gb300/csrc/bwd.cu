@@ -526,15 +526,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
               }
             }
             uint32_t pP[8], pS[8];  // [2 k + rh]: block kb + k, key row rh
-            // allowed query columns [clo, chi) of this thread's two key rows
-            // (an empty range for rows past the end of the sequence)
-            int clo[2], chi[2];
+            // allowed query columns [clo, clo + span) of this thread's two key
+            // rows (an empty range for rows past the end of the sequence)
+            int clo[2];
+            unsigned span[2];
 #pragma unroll
             for (int rh = 0; rh < 2; ++rh) {
               const int rr = 32 * quarter + 16 * grp + 8 * rh + gq;
               const int j = u.c0 + rr;
-              clo[rh] = rr < u.nkeys ? (p.causal ? j : 0) - qb : 0x7fffffff;
-              chi[rh] = p.window > 0 ? j + p.window - qb : 0x7fffffff;
+              clo[rh] = (p.causal ? j : 0) - qb;
+              const int chi = p.window > 0 ? j + p.window - qb : 0x40000000;
+              span[rh] = rr < u.nkeys ? (unsigned)max(chi - clo[rh], 0) : 0u;
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -544,10 +546,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 const float2 x = f2unpack(ffma2(f2pack(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])),
                                                 sl2x2, f2pack(a4[k].x, a4[k].y)));
                 float P0 = ex2(x.x), P1 = ex2(x.y);
-                if (kMask) {
+                if (kMask) {  // one unsigned compare and a select per element
                   const int col = 8 * (kb + k) + 2 * qq;
-                  if (col < clo[rh] || col >= chi[rh]) P0 = 0.f;
-                  if (col + 1 < clo[rh] || col + 1 >= chi[rh]) P1 = 0.f;
+                  P0 = (unsigned)(col - clo[rh]) < span[rh] ? P0 : 0.f;
+                  P1 = (unsigned)(col + 1 - clo[rh]) < span[rh] ? P1 : 0.f;
                 }
                 const uint64_t P = f2pack(P0, P1);
                 const uint64_t t = fmul2(P, f2pack(__uint_as_float(pv[cur][e]), __uint_as_float(pv[cur][e + 1])));

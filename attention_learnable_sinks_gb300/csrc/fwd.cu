@@ -311,10 +311,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tc_fence_before();
         mbar_arrive(&sm.s_empty);
         if (c0 < klo || c0 + kTile > khi) {
-          const int cl = klo - c0, ch = khi - c0;
+          // keys outside [cl, ch) get -inf; one unsigned compare and a select
+          // per element, no branches
+          const int cl = klo - c0;
+          const unsigned span = (unsigned)max(khi - klo, 0);
 #pragma unroll
-          for (int c = 0; c < kTile; ++c)
-            if (c < cl || c >= ch) s[c] = -INFINITY;
+          for (int c = 0; c < kTile; ++c) s[c] = (unsigned)(c - cl) < span ? s[c] : -INFINITY;
         }
         // row maximum with three-input max (two new values per instruction)
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
