@@ -376,11 +376,33 @@ def run_gb300(args):
     else:
         dom, dom_ms, dom_flops, dom_file = "fwd", f_avg, fwd_flops, "fwd.cu"
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
-    tr = traffic_record(dom_file)
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16 dense (burst)",
-                "traffic": tr["dram_bytes_per_launch"] if tr else None}
+    tr = traffic_record(dom_file) if args.workload == "dense" else None
+    if w.window > 0:
+        # a band of W keys: about W flop per byte moved, below the ridge
+        # (1910.8 TFLOP/s / 6786.6 GB/s = 282 flop/B), so HBM bounds it.
+        # Algorithmic bytes per launch, per token (d = 64):
+        #   forward:       read q, k, v; write o, LSE
+        #   backward main: read q, dO, k, v, LSE, D; write dk, dv and the fp32
+        #                  dq accumulator once
+        d, Hq, Hkv = 64, w.Hq, w.Hkv
+        per_tok = (2 * Hq * d + 4 * Hkv * d + 2 * Hq * d + 4 * Hq) if dom == "fwd" else \
+            (4 * Hq * d + 4 * Hkv * d + 8 * Hq + 4 * Hkv * d + 4 * Hq * d)
+        gbs = per_tok * w.total / (dom_ms / 1e3) / 1e9
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": gbs / hbm, "peak_source": f"{peak_src} HBM copy",
+                    "algorithmic_bytes_per_launch": per_tok * w.total,
+                    "tflops": achieved, "traffic": tr["dram_bytes_per_launch"] if tr else None}
+    else:
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": f"{peak_src} bf16 dense (burst)",
+                    "traffic": tr["dram_bytes_per_launch"] if tr else None}
+    # nominal dense bf16 rate of this GPU for context: SMs x max SM clock x
+    # 8192 flop/clk/SM (one M=128, N=256, K=16 product per 128 clk per SM)
+    props_n = torch.cuda.get_device_properties(device)
+    nominal = props_n.multi_processor_count * clk.get("sm_max_mhz", 0) * 1e6 * 8192 / 1e12 \
+        if clk.get("sm_max_mhz") else None
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -388,6 +410,8 @@ def run_gb300(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
         "config": workload_config(w, args.workload),
         "frac_of_peak": value / world / peak, "peak_tflops": peak, "peak_source": peak_src,
+        "peak_nominal_tflops": nominal,
+        "frac_of_nominal_peak": (value / world / nominal) if nominal else None,
         "fwd_ms": f_avg, "bwd_main_ms": b_avg,
         "fwd_tflops": fwd_flops / (f_avg / 1e3) / 1e12,
         "bwd_main_tflops": bwd_flops / (b_avg / 1e3) / 1e12,
