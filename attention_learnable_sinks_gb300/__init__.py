@@ -5,6 +5,6 @@ package is its thin PyTorch binding. Importing the package does not load the
 library; the first call does, and raises if it is missing.
 """
 
-from .api import backward, forward, sink_attention, workspace_bytes  # noqa: F401
+from .api import backward, decode, forward, sink_attention, workspace_bytes  # noqa: F401
 
 __all__ = ["sink_attention", "forward", "backward", "workspace_bytes"]

@@ -45,6 +45,19 @@ class BwdParams(ctypes.Structure):
     ]
 
 
+class DecodeParams(ctypes.Structure):
+    _fields_ = [
+        ("q", _c_void_p), ("k_cache", _c_void_p), ("v_cache", _c_void_p),
+        ("block_table", _c_void_p), ("seqlens", _c_void_p), ("sinks", _c_void_p),
+        ("o", _c_void_p), ("lse", _c_void_p),
+        ("workspace", _c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("nseq", ctypes.c_int32), ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float),
+    ]
+
+
 # Every symbol include/sinkattn.h declares: (name, restype, argtypes).
 SYMBOLS = [
     ("sinkattn_fwd_workspace_size", ctypes.c_size_t, [ctypes.c_int32] * 5),
@@ -52,6 +65,8 @@ SYMBOLS = [
     ("sinkattn_fwd", ctypes.c_int, [ctypes.POINTER(FwdParams), _c_void_p]),
     ("sinkattn_bwd", ctypes.c_int, [ctypes.POINTER(BwdParams), _c_void_p]),
     ("sinkattn_bwd_static_workspace", ctypes.c_int, [ctypes.POINTER(BwdParams), _c_void_p]),
+    ("sinkattn_decode_workspace_size", ctypes.c_size_t, [ctypes.c_int32] * 3),
+    ("sinkattn_decode", ctypes.c_int, [ctypes.POINTER(DecodeParams), _c_void_p]),
     ("sinkattn_status_string", ctypes.c_char_p, [ctypes.c_int32]),
     ("sinkattn_last_error_message", ctypes.c_char_p, []),
     ("sinkattn_device_error", ctypes.c_int32, [ctypes.c_int32]),
@@ -90,7 +105,8 @@ def lib():
             fn.restype = res
             fn.argtypes = args
         if L.sinkattn_params_size(0) != ctypes.sizeof(FwdParams) or \
-                L.sinkattn_params_size(1) != ctypes.sizeof(BwdParams):
+                L.sinkattn_params_size(1) != ctypes.sizeof(BwdParams) or \
+                L.sinkattn_params_size(2) != ctypes.sizeof(DecodeParams):
             raise RuntimeError("libsinkattn.so parameter structs do not match this binding")
         _lib = L
     return _lib

@@ -11,7 +11,7 @@ from typing import Optional, Sequence
 import torch
 
 from . import _binding
-from ._binding import BwdParams, FwdParams, check
+from ._binding import BwdParams, DecodeParams, FwdParams, check
 
 HEAD_DIM = 64
 
@@ -124,6 +124,51 @@ def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=Tru
     p.accumulate_dsinks = 1 if accumulate_dsinks else 0
     check(L.sinkattn_bwd(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_bwd")
     return dq, dk, dv, dsinks
+
+
+def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, scale=None,
+           num_splits=0, out=None, lse=None, workspace=None):
+    """One query row per sequence against a paged KV cache.
+
+    q [nseq, Hq, 64] bf16; k_cache, v_cache [num_blocks, block_size, Hkv, 64]
+    bf16; block_table [nseq, max_blocks] int32; seqlens [nseq] int32 (keys per
+    sequence, the new token's included). Returns o [nseq, Hq, 64] bf16 and
+    lse [Hq, nseq] fp32: the last row of ``forward`` over each sequence."""
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
+        raise ValueError("q must be [nseq, Hq, 64]")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.shape[3] != HEAD_DIM:
+        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, Hkv, 64]")
+    for name, t in (("block_table", block_table), ("seqlens", seqlens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    nseq, Hq, d = q.shape
+    if block_table.dim() != 2 or block_table.shape[0] != nseq or seqlens.shape != (nseq,):
+        raise ValueError("block_table must be [nseq, max_blocks] and seqlens [nseq]")
+    if sinks is not None and (sinks.dtype != torch.float32 or not sinks.is_cuda or
+                              sinks.shape != (Hq,) or not sinks.is_contiguous()):
+        raise ValueError("sinks must be a contiguous fp32 CUDA tensor [Hq]")
+    L = _binding.lib()
+    o = out if out is not None else torch.empty(nseq, Hq, d, dtype=torch.bfloat16, device=q.device)
+    lse = lse if lse is not None else torch.empty(Hq, nseq, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = L.sinkattn_decode_workspace_size(nseq, Hq, num_splits if num_splits > 0 else 64)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    p = DecodeParams()
+    p.q, p.k_cache, p.v_cache = _ptr(q), _ptr(k_cache), _ptr(v_cache)
+    p.block_table, p.seqlens, p.sinks = _ptr(block_table), _ptr(seqlens), _ptr(sinks)
+    p.o, p.lse = _ptr(o), _ptr(lse)
+    p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
+    p.nseq, p.num_blocks, p.block_size = nseq, k_cache.shape[0], k_cache.shape[1]
+    p.max_blocks_per_seq = block_table.shape[1]
+    p.Hq, p.Hkv, p.head_dim = Hq, k_cache.shape[2], d
+    p.window = int(window)
+    p.num_splits = int(num_splits)
+    p.softmax_scale = float(scale) if scale is not None else 0.0
+    check(L.sinkattn_decode(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_decode")
+    return o, lse
 
 
 def workspace_bytes(kind: str, nseq: int, total: int, Hq: int, Hkv: int) -> int:

@@ -1,6 +1,7 @@
 // C ABI of libsinkattn.so (declared in include/sinkattn.h): argument checks,
 // workspace layout and the order of kernel launches. No device memory is
 // allocated here; every buffer, workspace included, belongs to the caller.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -187,12 +188,12 @@ void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_re
 void note_error_message(const std::string& msg) { g_message = msg; }
 
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
-                                int64_t row_stride) {
+                                int64_t row_stride, int box_rows) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)total};
   const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)row_stride * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kTile};
+  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)box_rows};
   const cuuint32_t elem[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -311,6 +312,82 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   return SINKATTN_OK;
 }
 
+size_t sinkattn_decode_workspace_size(int32_t nseq, int32_t Hq, int32_t num_splits) {
+  if (nseq < 0 || Hq <= 0 || Hq > 65535 || num_splits < 1 || num_splits > 64) return 0;
+  return decode_workspace_bytes(nseq, Hq, num_splits);
+}
+
+sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
+  g_message.clear();
+  if (!a) return fail(SINKATTN_ERR_INVALID_ARG, "params is NULL");
+  if (a->head_dim != kHeadDim) return fail(SINKATTN_ERR_UNSUPPORTED, "head_dim must be 64");
+  if (a->nseq < 0 || a->nseq > 65535 || a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv || a->Hq > 65535)
+    return fail(SINKATTN_ERR_INVALID_ARG, "need 0 <= nseq <= 65535, 0 < Hkv, Hq % Hkv == 0, Hq <= 65535");
+  const int G = a->Hq / a->Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(SINKATTN_ERR_UNSUPPORTED, "Hq / Hkv must be 1, 2, 4, 8 or 16");
+  if (a->block_size != 16 && a->block_size != 32 && a->block_size != 64 && a->block_size != 128)
+    return fail(SINKATTN_ERR_UNSUPPORTED, "block_size must be 16, 32, 64 or 128");
+  if (a->num_blocks <= 0 || a->max_blocks_per_seq <= 0 ||
+      (int64_t)a->num_blocks * a->block_size > INT32_MAX ||
+      (int64_t)a->max_blocks_per_seq * a->block_size > INT32_MAX)
+    return fail(SINKATTN_ERR_INVALID_ARG, "num_blocks and max_blocks_per_seq must be > 0 and cover < 2^31 tokens");
+  if (a->num_splits < 0 || a->num_splits > 64)
+    return fail(SINKATTN_ERR_INVALID_ARG, "num_splits must be in [0, 64]");
+  if (std::isnan(a->softmax_scale) || std::isinf(a->softmax_scale))
+    return fail(SINKATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (a->nseq == 0) return SINKATTN_OK;
+  if (!a->q || !a->k_cache || !a->v_cache || !a->block_table || !a->seqlens || !a->o)
+    return fail(SINKATTN_ERR_INVALID_ARG, "q, k_cache, v_cache, block_table, seqlens and o must be non-NULL");
+  if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->o))
+    return fail(SINKATTN_ERR_INVALID_ARG, "q, the caches and o must be 16-byte aligned");
+  if (!a->workspace ||
+      a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, std::max(a->num_splits, 1)))
+    return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_decode_workspace_size()");
+  int sms = 0;
+  DecodeProblem p{};
+  sinkattn_status st = device_info(&p.err, &sms);
+  if (st != SINKATTN_OK) return st;
+  // Split count: enough CTAs for two per SM, at most one split per 128-key
+  // chunk a sequence can have, and no more than the workspace holds.
+  const int64_t keys = (int64_t)a->max_blocks_per_seq * a->block_size;
+  const int64_t span = a->window > 0 ? std::min<int64_t>(keys, (int64_t)a->window + 128) : keys;
+  const int64_t chunks = std::max<int64_t>(1, (span + 127) / 128);
+  int nsplit = a->num_splits;
+  if (nsplit == 0) {
+    const int64_t units = (int64_t)a->nseq * a->Hkv;
+    nsplit = (int)std::min<int64_t>({64, chunks, std::max<int64_t>(1, (2 * sms + units - 1) / units)});
+    while (nsplit > 1 && decode_workspace_bytes(a->nseq, a->Hq, nsplit) > a->workspace_bytes) --nsplit;
+  }
+  if (a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, nsplit))
+    return fail(SINKATTN_ERR_WORKSPACE, "workspace smaller than sinkattn_decode_workspace_size()");
+  char* ws = static_cast<char*>(a->workspace);
+  const size_t n = (size_t)a->nseq * a->Hq * nsplit;
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.k_cache = static_cast<const __nv_bfloat16*>(a->k_cache);
+  p.v_cache = static_cast<const __nv_bfloat16*>(a->v_cache);
+  p.block_table = a->block_table;
+  p.seqlens = a->seqlens;
+  p.sinks = a->sinks;
+  p.o = static_cast<__nv_bfloat16*>(a->o);
+  p.lse = a->lse;
+  p.part_ml = reinterpret_cast<float*>(ws);
+  p.part_o = reinterpret_cast<float*>(ws + align256(n * 2 * sizeof(float)));
+  p.nseq = a->nseq;
+  p.num_blocks = a->num_blocks;
+  p.block_size = a->block_size;
+  p.max_blocks = a->max_blocks_per_seq;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.window = a->window > 0 ? a->window : 0;
+  p.nsplit = nsplit;
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernels");
+  return SINKATTN_OK;
+}
+
 const char* sinkattn_status_string(int32_t status) {
   switch (status) {
     case SINKATTN_OK: return "ok";
@@ -346,6 +423,7 @@ uint64_t sinkattn_launch_count(void) { return g_launches.load(); }
 size_t sinkattn_params_size(int32_t which) {
   if (which == 0) return sizeof(sinkattn_fwd_params);
   if (which == 1) return sizeof(sinkattn_bwd_params);
+  if (which == 2) return sizeof(sinkattn_decode_params);
   return 0;
 }
 

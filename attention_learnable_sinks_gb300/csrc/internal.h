@@ -45,6 +45,23 @@ struct BwdProblem {
   int32_t accumulate_dsinks;   // add to dsinks instead of overwriting it
 };
 
+// Decode over a paged KV cache, as the kernels see it.
+struct DecodeProblem {
+  const __nv_bfloat16* q;        // [nseq, Hq, 64]
+  const __nv_bfloat16* k_cache;  // [num_blocks, block_size, Hkv, 64]
+  const __nv_bfloat16* v_cache;
+  const int32_t* block_table;    // [nseq, max_blocks]
+  const int32_t* seqlens;        // [nseq]
+  const float* sinks;            // null: no sink
+  __nv_bfloat16* o;              // [nseq, Hq, 64]
+  float* lse;                    // [Hq, nseq] or null
+  float* part_ml;                // [nseq, Hq, nsplit, 2] workspace: running max (log2 units), sum
+  float* part_o;                 // [nseq, Hq, nsplit, 64] workspace: unnormalised output
+  int32_t nseq, num_blocks, block_size, max_blocks, Hq, Hkv, window, nsplit;
+  float scale_log2;              // softmax scale * log2(e)
+  int32_t* err;                  // device error word
+};
+
 // Tile work list in the workspace: meta[0] = number of items, meta[1] = the
 // next item to hand out (work stealing), items[] = {sequence, tile} sorted by
 // decreasing cost.
@@ -76,9 +93,9 @@ __host__ __device__ inline void seeing_rows(int causal, int window, int L, int c
 }
 
 // TMA descriptor for a bf16 [total, heads, 64] token-major tensor (row stride
-// in elements): 3-D {64, heads, total}, 128-byte swizzle, box {64, 1, 128}.
+// in elements): 3-D {64, heads, total}, 128-byte swizzle, box {64, 1, box_rows}.
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
-                                int64_t row_stride);
+                                int64_t row_stride, int box_rows = kTile);
 
 // TMA descriptor for the fp32 [total, heads, 64] dq accumulator (contiguous):
 // 3-D {64, heads, total}, 128-byte swizzle, box {32, 1, 128}.
@@ -93,6 +110,9 @@ cudaError_t launch_bwd_main(const BwdProblem& p, const TileList& ktiles, int num
                             cudaStream_t s);
 cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int num_sms,
                               cudaStream_t s);
+
+size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit);
+cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t s);
 
 // Counts kernel launches (sinkattn_launch_count).
 void note_launch(int n = 1);

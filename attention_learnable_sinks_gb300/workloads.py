@@ -133,3 +133,99 @@ DESCRIPTIONS = {
 
 def config(name: str) -> Workload:
     return make(name, **CONFIGS[name])
+
+
+@dataclass
+class DecodeWorkload:
+    """One decode step: a query row per sequence over a paged KV cache.
+
+    Cache slots that hold no key of any sequence (the tail of each sequence's
+    last block, spare blocks) are NaN, so a kernel that reads them where it
+    should not shows it in its output."""
+    name: str
+    q: torch.Tensor            # bf16 [nseq, Hq, d]
+    k_cache: torch.Tensor      # bf16 [num_blocks, block_size, Hkv, d]
+    v_cache: torch.Tensor      # bf16 [num_blocks, block_size, Hkv, d]
+    block_table: torch.Tensor  # int32 [nseq, max_blocks], -1 past a sequence's blocks
+    seqlens: torch.Tensor      # int32 [nseq]
+    sinks: torch.Tensor        # fp32 [Hq]
+    window: int = 0
+    scale: float = HEAD_DIM ** -0.5
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def nseq(self) -> int:
+        return int(self.seqlens.numel())
+
+    @property
+    def Hq(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def Hkv(self) -> int:
+        return int(self.k_cache.shape[2])
+
+    @property
+    def block_size(self) -> int:
+        return int(self.k_cache.shape[1])
+
+
+def make_decode(name: str, lengths, Hq: int, Hkv: int, block_size: int, *, seed: int,
+                window: int = 0, qk_std: float = 1.0, sink_range=(-2.0, 2.0),
+                odd_head_sink=None, spare_blocks: int = 3, extra_columns: int = 1,
+                d: int = HEAD_DIM) -> DecodeWorkload:
+    """Draw one decode step. Order: lengths -> q -> keys -> values -> sinks ->
+    the permutation that places logical blocks in physical ones."""
+    g = torch.Generator().manual_seed(seed)
+    if callable(lengths):
+        lengths = lengths(g)
+    lengths = [int(x) for x in lengths]
+    nseq, total = len(lengths), sum(lengths)
+    nblk = [(L + block_size - 1) // block_size for L in lengths]
+    num_blocks = sum(nblk) + spare_blocks
+    max_blocks = max(nblk + [0]) + extra_columns
+    q = (torch.randn(nseq, Hq, d, generator=g) * qk_std).to(torch.bfloat16)
+    k_tok = (torch.randn(total, Hkv, d, generator=g) * qk_std).to(torch.bfloat16)
+    v_tok = torch.randn(total, Hkv, d, generator=g).to(torch.bfloat16)
+    lo, hi = sink_range
+    sinks = torch.rand(Hq, generator=g, dtype=torch.float32) * (hi - lo) + lo
+    if odd_head_sink is not None:
+        sinks[1::2] = odd_head_sink
+    perm = torch.randperm(num_blocks, generator=g)
+    nan = float("nan")
+    k_cache = torch.full((num_blocks, block_size, Hkv, d), nan, dtype=torch.bfloat16)
+    v_cache = torch.full((num_blocks, block_size, Hkv, d), nan, dtype=torch.bfloat16)
+    table = torch.full((nseq, max_blocks), -1, dtype=torch.int32)
+    nxt, off = 0, 0
+    for b, L in enumerate(lengths):
+        for i in range(nblk[b]):
+            pb = int(perm[nxt])
+            nxt += 1
+            table[b, i] = pb
+            n = min(block_size, L - i * block_size)
+            k_cache[pb, :n] = k_tok[off + i * block_size: off + i * block_size + n]
+            v_cache[pb, :n] = v_tok[off + i * block_size: off + i * block_size + n]
+        off += L
+    meta = {"lengths": lengths, "seed": seed, "k_tokens": k_tok, "v_tokens": v_tok}
+    return DecodeWorkload(name, q, k_cache, v_cache, table,
+                          torch.tensor(lengths, dtype=torch.int32), sinks, window, d ** -0.5, meta)
+
+
+def _decode_lengths(g):
+    return torch.randint(256, 8192 + 1, (64,), generator=g).tolist()
+
+
+DECODE_CONFIGS = {
+    "decode": dict(lengths=_decode_lengths, Hq=64, Hkv=8, block_size=64, seed=6),
+    "decode_window": dict(lengths=_decode_lengths, Hq=64, Hkv=8, block_size=64, seed=6,
+                          window=128, sink_range=(-4.0, 4.0)),
+}
+
+DECODE_DESCRIPTIONS = {
+    "decode": "64 seqs L~U[256,8192] Hq=64 Hkv=8 d=64, paged cache of 64-token blocks",
+    "decode_window": "as decode, window=128",
+}
+
+
+def decode_config(name: str) -> DecodeWorkload:
+    return make_decode(name, **DECODE_CONFIGS[name])

@@ -9,12 +9,15 @@ pairs the mask allows: forward 4*d per pair and head, backward 10*d
 (five products), so a step is 14*d*N_pairs*Hq.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload dense|window|varlen|long|long_window|tiny]
+                    [--workload dense|window|varlen|long|long_window|tiny|decode|decode_window]
 
 For N > 1 launch under torch.distributed.run: every rank runs its own batch
 (no collective on the data path), timing is the max over ranks, and value is
 the total over ranks. --impl reference times the fp64 CPU oracle on a
 bounded sample of the same workload (rank 0 only).
+
+The decode workloads time one decode step (a query row per sequence over a
+paged KV cache) instead, reported as algorithmic HBM GB/s.
 """
 
 from __future__ import annotations
@@ -437,6 +440,188 @@ def run_gb300(args):
     return 0
 
 
+# ----------------------------------------------------------------- decode
+DECODE_METRIC = "sink-attn paged decode, algorithmic HBM GB/s on 1 GB300 and % of measured copy bandwidth"
+
+
+def decode_bytes(w):
+    """Algorithmic bytes of one decode step: the visible keys' K and V rows,
+    q and o (bf16), LSE (fp32). Block rounding and the split partials are
+    overhead, not counted."""
+    d = HEAD_DIM
+    keys = sum(min(L, w.window) if w.window > 0 else L for L in w.meta["lengths"])
+    return keys * w.Hkv * d * 2 * 2 + w.nseq * w.Hq * (2 * d * 2 + 4)
+
+
+def decode_config_record(w, name):
+    from attention_learnable_sinks_gb300.workloads import DECODE_DESCRIPTIONS
+    return {"workload": f"{name}: {DECODE_DESCRIPTIONS[name]}", "nseq": w.nseq,
+            "cached_tokens": sum(w.meta["lengths"]), "Hq": w.Hq, "Hkv": w.Hkv,
+            "head_dim": HEAD_DIM, "block_size": w.block_size, "window": w.window,
+            "l2": "flushed between timed steps (512 MiB write)",
+            "byte_convention": "visible K,V rows + q + o + lse per step"}
+
+
+_F64_CACHE = {}
+
+
+def oracle_decode_sample(w, seqs):
+    """Time the fp64 decode oracle on some sequences (the caches are converted
+    to fp64 once, outside the timing). Returns (seconds, algorithmic bytes)."""
+    from oracle import decode as odec
+
+    def f64(t):
+        return t.float().numpy().astype(np.float64)
+    if id(w) not in _F64_CACHE:
+        _F64_CACHE.clear()
+        _F64_CACHE[id(w)] = (f64(w.k_cache), f64(w.v_cache))
+    kc, vc = _F64_CACHE[id(w)]
+    q = f64(w.q[seqs])
+    t0 = time.perf_counter()
+    odec.decode(q, kc, vc, w.block_table.numpy()[seqs], w.seqlens.numpy()[seqs], w.sinks.numpy(),
+                window=w.window, scale=w.scale)
+    dt = time.perf_counter() - t0
+    d = HEAD_DIM
+    lens = [w.meta["lengths"][b] for b in seqs]
+    keys = sum(min(L, w.window) if w.window > 0 else L for L in lens)
+    return dt, keys * w.Hkv * d * 4 + len(seqs) * w.Hq * (4 * d + 4)
+
+
+def run_decode(args):
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        from attention_learnable_sinks_gb300 import workloads
+        w = workloads.decode_config(args.workload)
+        seqs = [0, 1]
+        for _ in range(args.warmup):
+            oracle_decode_sample(w, seqs)
+        secs, nbytes = 0.0, 0
+        for _ in range(args.steps):
+            dt, b = oracle_decode_sample(w, seqs)
+            secs += dt
+            nbytes += b
+        value = nbytes / secs / 1e9
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded)", "config": decode_config_record(w, args.workload),
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"numpy fp64 decode oracle, sequences {seqs}"},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line))
+        return 0
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from attention_learnable_sinks_gb300 import _binding, api, workloads
+    _binding.lib()
+    w = workloads.decode_config(args.workload)
+    q, kc, vc = w.q.to(device), w.k_cache.to(device), w.v_cache.to(device)
+    table, lens, s = w.block_table.to(device), w.seqlens.to(device), w.sinks.to(device)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.Hq, w.nseq, dtype=torch.float32, device=device)
+    ws = torch.empty(_binding.lib().sinkattn_decode_workspace_size(w.nseq, w.Hq, 64),
+                     dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    nbytes = decode_bytes(w)
+
+    def step():
+        api.decode(q, kc, vc, table, lens, s, window=w.window, scale=w.scale, out=o, lse=lse,
+                   workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert _binding.device_error() == 0, "device error word set during warm-up"
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    props = torch.cuda.get_device_properties(device)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    n0 = _binding.launch_count()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = _binding.launch_count() - n0
+    clk = clocks.stop()
+    assert _binding.device_error() == 0, "device error word set during the timed region"
+    total_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), world, device)
+    ms = total_ms / K
+    value = nbytes * world * K / (total_ms / 1e3) / 1e9
+
+    # end to end: the cache is state that stays on the device; each step copies
+    # the new query rows and lengths in and o, lse out through pinned buffers
+    hq, hl = w.q.pin_memory(), w.seqlens.pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = hq.numel() * 2 + hl.numel() * 4
+    d2h = ho.numel() * 2 + hlse.numel() * 4
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        lens.copy_(hl, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        e2e_ev[i][0].record()
+        e2e_step()
+        e2e_ev[i][1].record()
+    torch.cuda.synchronize()
+    e2e_total = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, device)
+    e2e_value = nbytes * world * K / (e2e_total / 1e3) / 1e9
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": decode_config_record(w, args.workload),
+        "sequences_per_s": w.nseq * world * K / (total_ms / 1e3),
+        "roofline": {"bound": "hbm", "kernel": "decode (split + combine)", "achieved": value / world,
+                     "peak": hbm, "unit": "GB/s", "frac": value / world / hbm,
+                     "peak_source": f"{peak_src} HBM copy",
+                     "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, b = oracle_decode_sample(w, [0, 1, 2, 3])
+        line["cpu_baseline"] = {"value": b / secs / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "seconds": secs,
+                                "sample": f"numpy fp64 decode oracle, sequences 0-3 of {args.workload}"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,13 +629,16 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", default="dense",
-                    choices=("tiny", "dense", "window", "varlen", "long", "long_window"))
+                    choices=("tiny", "dense", "window", "varlen", "long", "long_window",
+                             "decode", "decode_window"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=2,
                     help="groups of whole sequences streamed by the end-to-end leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.workload.startswith("decode"):
+        return run_decode(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gb300(args)

@@ -160,6 +160,63 @@ SINKATTN_API sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* params, voi
 SINKATTN_API sinkattn_status sinkattn_bwd_static_workspace(const sinkattn_bwd_params* params,
                                                            void* stream);
 
+/* Decode: one new query row per sequence against a paged KV cache, the
+ * inference side of the same attention (page "GPT-OSS Agentic RL Training: A
+ * Practical Retrospective", section "Implementation in FlashAttention v3",
+ * step 1: the forward with sinks, which the pages took from an inference
+ * engine). Sequence b holds seqlens[b] keys, the new token's included, and its
+ * query is the row at the last position: it sees keys j in
+ * [max(0, L - window), L) (all L keys when window <= 0), plus the sink of its
+ * head, so o and lse equal the last row of sinkattn_fwd over the same keys.
+ * The keys are split into up to num_splits ranges processed side by side;
+ * the partial results are merged with the sink in a second kernel.
+ *
+ * Layouts:
+ *   q            bf16 [nseq, Hq, 64] contiguous
+ *   k_cache,     bf16 [num_blocks, block_size, Hkv, 64] contiguous; logical
+ *   v_cache      block i of sequence b is physical block block_table[b][i]
+ *   block_table  int32 [nseq, max_blocks_per_seq]; entries for blocks past a
+ *                sequence's last key or wholly before its window are ignored,
+ *                the others must be in [0, num_blocks)
+ *   seqlens      int32 [nseq], 0 <= seqlens[b] <= max_blocks_per_seq * block_size
+ *   o            bf16 [nseq, Hq, 64] (out)
+ *   lse          fp32 [Hq, nseq] natural log (out; may be NULL)
+ * block_size must be 16, 32, 64 or 128; Hq / Hkv must be 1, 2, 4, 8 or 16.
+ * A sequence with no keys gets o = 0 and lse = S_h (the sink alone). Device
+ * pointers must be 16-byte aligned, the caches' too. An out-of-range length
+ * or block index found on the device sets the device error word
+ * (SINKATTN_ERR_INVALID_ARG) and that sequence's outputs are left unwritten. */
+typedef struct sinkattn_decode_params {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* seqlens;
+  const float* sinks;          /* fp32 [Hq]; NULL = no sink                    */
+  void* o;
+  float* lse;
+  void* workspace;             /* >= sinkattn_decode_workspace_size() bytes    */
+  size_t workspace_bytes;
+  int32_t nseq;                /* 0..65535                                     */
+  int32_t num_blocks;          /* > 0 physical blocks in each cache            */
+  int32_t block_size;          /* tokens per block                             */
+  int32_t max_blocks_per_seq;  /* columns of block_table                       */
+  int32_t Hq;
+  int32_t Hkv;
+  int32_t head_dim;            /* must be 64                                   */
+  int32_t window;              /* <= 0: every key; W > 0: the last W keys      */
+  int32_t num_splits;          /* key ranges per sequence, 1..64; 0 = choose    */
+  float softmax_scale;         /* <= 0 selects 1/sqrt(head_dim)                */
+} sinkattn_decode_params;
+
+/* Workspace bytes for a decode problem (0 on bad input). */
+SINKATTN_API size_t sinkattn_decode_workspace_size(int32_t nseq, int32_t Hq, int32_t num_splits);
+
+/* Enqueue the decode on `stream`. num_splits = 0 picks the split count from
+ * the shape (nseq, Hkv, max_blocks_per_seq * block_size) and the SM count;
+ * size the workspace for 64 splits then (or query it with the chosen count). */
+SINKATTN_API sinkattn_status sinkattn_decode(const sinkattn_decode_params* params, void* stream);
+
 /* Static description of a status code; never NULL. */
 SINKATTN_API const char* sinkattn_status_string(int32_t status);
 
@@ -175,7 +232,8 @@ SINKATTN_API int32_t sinkattn_device_error(int32_t reset);
 SINKATTN_API uint64_t sinkattn_launch_count(void);
 
 /* sizeof(sinkattn_fwd_params) for which = 0, sizeof(sinkattn_bwd_params) for
- * which = 1, else 0: lets a binding check its mirror of the structs. */
+ * which = 1, sizeof(sinkattn_decode_params) for which = 2, else 0: lets a
+ * binding check its mirror of the structs. */
 SINKATTN_API size_t sinkattn_params_size(int32_t which);
 
 #ifdef __cplusplus

@@ -9,7 +9,7 @@ import re
 import pytest
 
 from attention_learnable_sinks_gb300 import _binding
-from attention_learnable_sinks_gb300._binding import BwdParams, FwdParams
+from attention_learnable_sinks_gb300._binding import BwdParams, DecodeParams, FwdParams
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -22,7 +22,7 @@ def declared_functions():
 def test_library_exports_every_declared_symbol():
     lib = _binding.lib()
     names = declared_functions()
-    assert len(names) >= 9
+    assert len(names) >= 11
     bound = {n for n, _, _ in _binding.SYMBOLS}
     for n in names:
         assert hasattr(lib, n), f"{n} not exported"
@@ -33,7 +33,8 @@ def test_param_struct_sizes_match():
     lib = _binding.lib()
     assert lib.sinkattn_params_size(0) == ctypes.sizeof(FwdParams)
     assert lib.sinkattn_params_size(1) == ctypes.sizeof(BwdParams)
-    assert lib.sinkattn_params_size(2) == 0
+    assert lib.sinkattn_params_size(2) == ctypes.sizeof(DecodeParams)
+    assert lib.sinkattn_params_size(3) == 0
 
 
 def test_workspace_sizes():
@@ -126,3 +127,62 @@ def test_sequence_groups_for_the_host_pipeline():
     assert b[0] == 0 and b[-1] == 5 and all(x < y for x, y in zip(b, b[1:]))
     # a windowed cost grows linearly, so equal lengths still split evenly
     assert _split_sequences([1000] * 6, True, 128, 3) == [0, 2, 4, 6]
+
+
+def _decode_params(**kw):
+    p = DecodeParams()
+    fake = 0x10000  # never dereferenced: every case below fails or returns before a launch
+    p.q = p.k_cache = p.v_cache = p.block_table = p.seqlens = p.o = p.lse = fake
+    p.nseq, p.num_blocks, p.block_size, p.max_blocks_per_seq = 2, 8, 16, 4
+    p.Hq, p.Hkv, p.head_dim, p.window, p.num_splits = 8, 2, 64, 0, 0
+    buf = (ctypes.c_uint8 * 4096)()
+    p.workspace, p.workspace_bytes = ctypes.addressof(buf), 4096
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p, buf
+
+
+@pytest.mark.parametrize("change,status", [
+    ({"head_dim": 128}, 2),
+    ({"Hq": 6, "Hkv": 2}, 2),      # group of 3
+    ({"Hq": 64, "Hkv": 2}, 2),     # group of 32
+    ({"Hkv": 3}, 1),
+    ({"nseq": 65536}, 1),
+    ({"block_size": 8}, 2),
+    ({"block_size": 256}, 2),
+    ({"num_blocks": 0}, 1),
+    ({"max_blocks_per_seq": 0}, 1),
+    ({"num_blocks": 1 << 27, "block_size": 16}, 1),  # 2^31 cache rows
+    ({"num_splits": 65}, 1),
+    ({"num_splits": -1}, 1),
+    ({"softmax_scale": float("inf")}, 1),
+    ({"q": None}, 1),
+    ({"block_table": None}, 1),
+    ({"k_cache": 0x10004}, 1),     # not 16-byte aligned
+    ({"workspace": None}, 4),
+    ({"num_splits": 64, "workspace_bytes": 64}, 4),
+])
+def test_decode_rejects_bad_arguments(change, status):
+    lib = _binding.lib()
+    n0 = lib.sinkattn_launch_count()
+    p, buf = _decode_params(**change)
+    assert lib.sinkattn_decode(ctypes.byref(p), None) == status
+    assert lib.sinkattn_last_error_message()
+    assert lib.sinkattn_launch_count() == n0
+
+
+def test_decode_without_sequences_needs_no_device():
+    lib = _binding.lib()
+    p, buf = _decode_params(nseq=0, q=None, workspace=None)
+    assert lib.sinkattn_decode(ctypes.byref(p), None) == 0
+    assert lib.sinkattn_decode(None, None) == 1
+
+
+def test_decode_workspace_size():
+    lib = _binding.lib()
+    one = lib.sinkattn_decode_workspace_size(64, 64, 1)
+    assert one >= 64 * 64 * (2 + 64) * 4
+    assert lib.sinkattn_decode_workspace_size(64, 64, 8) >= 8 * 64 * 64 * 66 * 4
+    assert lib.sinkattn_decode_workspace_size(64, 64, 0) == 0
+    assert lib.sinkattn_decode_workspace_size(64, 64, 65) == 0
+    assert lib.sinkattn_decode_workspace_size(-1, 64, 1) == 0
