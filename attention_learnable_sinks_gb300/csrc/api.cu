@@ -348,17 +348,31 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
   DecodeProblem p{};
   sinkattn_status st = device_info(&p.err, &sms);
   if (st != SINKATTN_OK) return st;
-  // Split count: enough CTAs for two per SM, at most one split per 128-key
-  // chunk a sequence can have, and no more than the workspace holds.
+  // Splits: each takes `per` 128-key chunks. A sequence has at most `maxch`
+  // chunks (its keys from the 128-aligned chunk holding the window's first
+  // key). Automatic choice, from measurements on GB300: one split when a
+  // sequence spans at most 4 chunks (the split kernel then finishes the rows
+  // itself, without the combine pass); otherwise at least 4 splits, and enough
+  // CTAs for about 4 per SM, at most 64 splits and never less than 2 chunks
+  // each; fewer if the workspace is smaller.
   const int64_t keys = (int64_t)a->max_blocks_per_seq * a->block_size;
-  const int64_t span = a->window > 0 ? std::min<int64_t>(keys, (int64_t)a->window + 128) : keys;
-  const int64_t chunks = std::max<int64_t>(1, (span + 127) / 128);
-  int nsplit = a->num_splits;
-  if (nsplit == 0) {
+  const int64_t span = a->window > 0 ? std::min<int64_t>(keys, (int64_t)a->window + 127) : keys;
+  const int64_t maxch = std::max<int64_t>(1, (span + 127) / 128);
+  int64_t per;
+  if (a->num_splits > 0) {
+    per = (maxch + a->num_splits - 1) / a->num_splits;
+  } else if (maxch <= 4) {
+    per = maxch;
+  } else {
     const int64_t units = (int64_t)a->nseq * a->Hkv;
-    nsplit = (int)std::min<int64_t>({64, chunks, std::max<int64_t>(1, (2 * sms + units - 1) / units)});
-    while (nsplit > 1 && decode_workspace_bytes(a->nseq, a->Hq, nsplit) > a->workspace_bytes) --nsplit;
+    int64_t want = std::max<int64_t>(4, (4 * (int64_t)sms + units - 1) / units);
+    want = std::min<int64_t>({want, 64, std::max<int64_t>(1, maxch / 2)});
+    per = (maxch + want - 1) / want;
+    while ((maxch + per - 1) / per > 1 &&
+           decode_workspace_bytes(a->nseq, a->Hq, (int)((maxch + per - 1) / per)) > a->workspace_bytes)
+      ++per;
   }
+  const int nsplit = (int)((maxch + per - 1) / per);
   if (a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, nsplit))
     return fail(SINKATTN_ERR_WORKSPACE, "workspace smaller than sinkattn_decode_workspace_size()");
   char* ws = static_cast<char*>(a->workspace);
@@ -381,6 +395,7 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
   p.Hkv = a->Hkv;
   p.window = a->window > 0 ? a->window : 0;
   p.nsplit = nsplit;
+  p.split_chunks = (int32_t)per;
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
   p.scale_log2 = scale * 1.4426950408889634f;
   const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream));

@@ -57,7 +57,9 @@ struct DecodeProblem {
   float* lse;                    // [Hq, nseq] or null
   float* part_ml;                // [nseq, Hq, nsplit, 2] workspace: running max (log2 units), sum
   float* part_o;                 // [nseq, Hq, nsplit, 64] workspace: unnormalised output
-  int32_t nseq, num_blocks, block_size, max_blocks, Hq, Hkv, window, nsplit;
+  int32_t nseq, num_blocks, block_size, max_blocks, Hq, Hkv, window;
+  int32_t nsplit;                // splits per sequence (grid x)
+  int32_t split_chunks;          // 128-key chunks per split
   float scale_log2;              // softmax scale * log2(e)
   int32_t* err;                  // device error word
 };

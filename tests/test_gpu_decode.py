@@ -155,10 +155,12 @@ def test_bad_length_or_block_sets_the_device_error(cuda_lib):
     compare(w, got, ref, seqs=[0, 1])
 
 
-def test_decode_config_sampled(cuda_lib):
-    """The benchmarked decode workload at full size, checked on a sample of
-    sequences (the oracle is exact per sequence)."""
-    w = decode_config("decode_window")
+@pytest.mark.parametrize("name", ["decode", "decode_window"])
+def test_decode_config_sampled(cuda_lib, name):
+    """The benchmarked decode workloads at full size, in the launch the
+    benchmark times (automatic split count), checked on a sample of sequences
+    (the oracle is exact per sequence)."""
+    w = decode_config(name)
     got = run_cuda(w)
     assert _binding.device_error(reset=True) == 0
     pick = [0, 7, 31, 63]
