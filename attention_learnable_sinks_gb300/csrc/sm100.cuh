@@ -80,30 +80,17 @@ struct Guard {
   }
 };
 
-// As mbar_try_wait, but the thread may sleep in hardware (up to about
-// kSuspendNs) until the phase completes, instead of spinning on issue slots
-// that co-resident warps need.
-constexpr uint32_t kSuspendNs = 100000;  // 0.1 ms
-
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait until the phase with the given parity has completed. Returns false on
-// timeout or abort.
+// timeout or abort. Each try_wait may suspend the thread for a short,
+// hardware-chosen time while the phase is incomplete; between tries the loop
+// checks the abort flag and the time limit. (An explicit 0.1 ms suspend hint
+// was measured about 1% slower on the backward; a pure test_wait spin was
+// slower still.)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Guard& g) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (g.aborted()) return false;
     if (global_ns() - t0 > kWaitLimitNs) {
       g.fail(kErrTimeout);

@@ -81,6 +81,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_sha(kernel_file: str):
+    """Hash of a kernel's source together with the shared device headers it
+    includes, so that a change to either invalidates recorded counters."""
+    csrc = os.path.join(ROOT, "attention_learnable_sinks_gb300", "csrc")
+    h = hashlib.sha256()
+    try:
+        for fn in (kernel_file, "sm100.cuh", "internal.h"):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    except OSError:
+        return None
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel_file: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, valid only while the kernel source is unchanged."""
@@ -90,10 +103,8 @@ def traffic_record(kernel_file: str):
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    src = os.path.join(ROOT, "attention_learnable_sinks_gb300", "csrc", kernel_file)
-    try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    except OSError:
+    sha = kernel_source_sha(kernel_file)
+    if sha is None:
         return None
     entry = rec.get(kernel_file)
     if not entry or entry.get("source_sha") != sha:
