@@ -47,6 +47,10 @@ constexpr float kRescale = 8.0f;  // log2 units
 constexpr int kSchedSlots = 4;
 constexpr int kSchedConsumers = 1 + 4;  // the UMMA warp and 4 softmax warps
 
+struct Unit {
+  int base, L, r0, nrows, h, kvh, kt0, kt1;
+};
+
 struct __align__(1024) Smem {
   uint8_t q[kTileBytes];
   uint8_t k[kKStages][kTileBytes];
@@ -56,14 +60,12 @@ struct __align__(1024) Smem {
   uint64_t q_full, q_empty, s_full, s_empty, p_full, o_done, drain;
   uint64_t sched_full[kSchedSlots], sched_empty[kSchedSlots];
   int32_t sched_unit[kSchedSlots];  // work unit handed out, -1 = no more work
+  Unit sched_u[kSchedSlots];         // ... decoded by the producer
+  float sched_sink[kSchedSlots];     // ... and its head's sink * log2(e) (-inf: none)
   uint32_t tmem_base;
   int abort;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-
-struct Unit {
-  int base, L, r0, nrows, h, kvh, kt0, kt1;
-};
 
 __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int w) {
   const int2 it = items[w / p.Hq];
@@ -83,16 +85,19 @@ __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int 
 }
 
 // Work units are handed out dynamically (longest first, from the device-built
-// list): the producer thread takes the next index with an atomic and
-// publishes it in a small ring; the UMMA thread and the softmax warps read the
-// ring in order. `lanes` = the calling lanes of the warp (all of them get the
-// same verdict).
+// list): the producer thread takes the next index with an atomic, decodes it
+// (the global loads of the tile list, cu_seqlens and the sink happen there,
+// ahead of time) and publishes it in a small ring; the UMMA warp and the
+// softmax warps read the ring in order. `lanes` = the calling lanes of the
+// warp (all of them get the same verdict).
 template <class SmemT>
 __device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g, bool arrive,
-                                         unsigned lanes) {
+                                         unsigned lanes, Unit& u, float& sink2) {
   const int s = n % kSchedSlots;
   if (!__all_sync(lanes, mbar_wait(&sm.sched_full[s], (n / kSchedSlots) & 1, g))) return -1;
   const int w = __shfl_sync(lanes, sm.sched_unit[s], 0);  // warp-uniform
+  u = sm.sched_u[s];
+  sink2 = sm.sched_sink[s];
   __syncwarp(lanes);
   if (arrive) mbar_arrive(&sm.sched_empty[s]);
   ++n;
@@ -179,13 +184,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // take the next unit and publish it (or -1 when the list is exhausted)
         int w = atomicAdd(&meta[1], 1);
         if (w >= nwork) w = -1;
+        Unit u{};
+        float sink2 = -INFINITY;
+        if (w >= 0) {
+          u = decode(p, items, w);
+          if (p.sinks) sink2 = p.sinks[u.h] * kLog2e;
+        }
         const int s = nsched % kSchedSlots;
         if (!mbar_wait(&sm.sched_empty[s], ((nsched / kSchedSlots) & 1) ^ 1, g)) break;
         sm.sched_unit[s] = w;
+        sm.sched_u[s] = u;
+        sm.sched_sink[s] = sink2;
         mbar_arrive(&sm.sched_full[s]);
         ++nsched;
         if (w < 0) break;
-        const Unit u = decode(p, items, w);
         if (!mbar_wait(&sm.q_empty, (nq & 1) ^ 1, g)) break;
         mbar_expect_tx(&sm.q_full, kTileBytes);
         tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base + u.r0);
@@ -238,9 +250,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     };
     uint32_t nsched = 0;
     while (ok) {
-      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
+      Unit u;
+      float sink2;
+      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu, u, sink2);
       if (w < 0) break;
-      const Unit u = decode(p, items, w);
       const int n = __shfl_sync(0xffffffffu, u.kt1 - u.kt0, 0);  // warp-uniform trip count
       if (!mbar_wait_warp(&sm.q_full, nq & 1, g)) break;
       ++nq;
@@ -284,17 +297,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     uint32_t nsf = 0, nod = 0, nsched = 0;
     bool ok = true;
     while (ok) {
-      const int w = next_unit(sm, nsched, g, lane == 0, 0xffffffffu);
-      if (w < 0) break;
-      const Unit u = decode(p, items, w);
-      const int n = u.kt1 - u.kt0;
-      const int i = u.r0 + r;
-      const int khi = p.causal ? min(i + 1, u.L) : u.L;
+      // the ring slot stays held until the epilogue, and the unit's fields
+      // are read from it where they are used (no registers held across the
+      // tile loop)
+      const int slot = nsched % kSchedSlots;
+      if (!mbar_wait_warp(&sm.sched_full[slot], (nsched / kSchedSlots) & 1, g)) break;
+      ++nsched;
+      if (sm.sched_unit[slot] < 0) break;  // no more work
+      const volatile Unit& uv = sm.sched_u[slot];
+      const int kt0 = uv.kt0;
+      const int n = uv.kt1 - kt0;
+      const float sink2 = sm.sched_sink[slot];
+      const int i = uv.r0 + r;
+      const int L = uv.L;
+      const int khi = p.causal ? min(i + 1, L) : L;
       const int klo = p.window > 0 ? max(0, i - p.window + 1) : 0;
-      float m = p.sinks ? p.sinks[u.h] * kLog2e : -INFINITY;
+      float m = sink2;  // -inf without sinks
       float l = p.sinks ? 1.f : 0.f;
       for (int jj = 0; jj < n; ++jj) {
-        const int c0 = (u.kt0 + jj) * kTile;
+        const int c0 = (kt0 + jj) * kTile;
         if (!mbar_wait_warp(&sm.s_full, nsf & 1, g)) {
           ok = false;
           break;
@@ -389,15 +410,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         for (int e = 0; e < 32; ++e)
           ob[e] = pack_bf16(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
       }
-      if (r < u.nrows) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.o + ((int64_t)(u.base + u.r0 + r) * p.Hq + u.h) * kHeadDim);
+      const int nrows = uv.nrows, row0 = uv.base + uv.r0, h = uv.h;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.sched_empty[slot]);  // the slot is no longer read
+      if (r < nrows) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)(row0 + r) * p.Hq + h) * kHeadDim);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
         if (p.lse)
-          p.lse[(int64_t)u.h * p.total + u.base + u.r0 + r] =
-              l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+          p.lse[(int64_t)h * p.total + row0 + r] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
       }
     }
   }
