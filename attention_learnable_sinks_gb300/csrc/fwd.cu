@@ -13,7 +13,7 @@
 // with the other's matrix products.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer: Q tile, then K tiles (3-stage ring, one tile
+//   warp 0      TMA producer: Q tile, then K tiles (2-stage ring, one tile
 //               ahead) and V tiles (2-stage ring); a K stage is released as
 //               soon as S = Q K^T completes, a V stage after O += P V
 //   warp 1      UMMA issuer: S = Q K^T (SS, K-major both) and O += P V (P from
@@ -36,7 +36,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 192;
-constexpr int kKStages = 3;
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB of bf16
 constexpr uint32_t kTmemCols = 256;
@@ -55,6 +55,7 @@ struct __align__(1024) Smem {
   uint8_t q[kTileBytes];
   uint8_t k[kKStages][kTileBytes];
   uint8_t v[kVStages][kTileBytes];
+  uint8_t ostage[4][32 * 128];  // per softmax warp: its 32 rows of O (bf16), 16-byte chunks swizzled
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t q_full, q_empty, s_full, s_empty, p_full, o_done, drain;
@@ -413,14 +414,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int nrows = uv.nrows, row0 = uv.base + uv.r0, h = uv.h;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sched_empty[slot]);  // the slot is no longer read
-      if (r < nrows) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)(row0 + r) * p.Hq + h) * kHeadDim);
+      // O rows through shared memory, so that each store instruction writes
+      // four whole 128-byte rows instead of 16 bytes of 32 rows
+      uint8_t* ost = sm.ostage[quarter];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-        if (p.lse)
-          p.lse[(int64_t)h * p.total + row0 + r] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(ost + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+            make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int rr = 4 * k + (lane >> 3), c = lane & 7;  // row of this warp, 16-byte chunk
+        const uint4 x = *reinterpret_cast<const uint4*>(ost + rr * 128 + ((c ^ (rr & 7)) << 4));
+        if (32 * quarter + rr < nrows)
+          reinterpret_cast<uint4*>(p.o + ((int64_t)(row0 + 32 * quarter + rr) * p.Hq + h) * kHeadDim)[c] = x;
       }
+      __syncwarp();
+      if (p.lse && r < nrows)
+        p.lse[(int64_t)h * p.total + row0 + r] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
