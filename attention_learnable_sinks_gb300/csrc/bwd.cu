@@ -481,9 +481,23 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const int hh = i / u.nq;
         const int qb = (u.qt0 + i % u.nq) * kTile + 64 * hf;
         const int st = ntile % kQStages, db = ntile & 1;
-        // the producer's LSE / D / p_sink rows of this tile (acquire)
-        if (!mbar_wait_warp(&sm.q_full[st], (ntile / kQStages) & 1, g) ||
-            !mbar_wait_warp(&sm.sdp_full[hf], nsd & 1, g)) {
+        // the producer's LSE / D / p_sink rows of this tile (acquire); the
+        // first half of this thread's per-query constants is read while
+        // S^T / dP^T are still being computed
+        if (!mbar_wait_warp(&sm.q_full[st], (ntile / kQStages) & 1, g)) {
+          ok = false;
+          break;
+        }
+        const float4* ld = &sm.rowld[st][32 * hf + qq];  // + 4 k: {-LSE*log2e x2, -D x2}
+        const float2* pp = &sm.rowps[st][32 * hf + qq];  // + 4 k: p_sink x2
+        float4 a4[4];
+        float2 b2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          a4[k] = ld[4 * k];
+          b2[k] = pp[4 * k];
+        }
+        if (!mbar_wait_warp(&sm.sdp_full[hf], nsd & 1, g)) {
           ok = false;
           break;
         }
@@ -494,8 +508,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const bool full =
             __all_sync(0xffffffffu, rows_valid && qb >= qlo_max && qb + 63 < qhi_min);
         const uint32_t srow = smem_u32(sm.dst[db] + hf * kTileBytes);
-        const float4* ld = &sm.rowld[st][32 * hf + qq];  // + 4 k: {-LSE*log2e x2, -D x2}
-        const float2* pp = &sm.rowps[st][32 * hf + qq];  // + 4 k: p_sink x2
         // chunk c: lane group c & 1, 8-column blocks kb .. kb + 3 (kb = 4 (c >> 1));
         // the TMEM loads of chunk c + 1 are in flight while chunk c is computed
         auto taddr = [&](int c, uint32_t col) {
@@ -506,8 +518,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         auto chunks = [&](auto mask_tag) {
           constexpr bool kMask = decltype(mask_tag)::value;
           uint32_t sv[2][16], pv[2][16];
-          float4 a4[4];
-          float2 b2[4];
           tmem_ld16x256b_x4x2_async(taddr(0, kColS + 64 * hf), taddr(0, kColDP + 64 * hf), sv[0], pv[0]);
           tmem_ld_wait();
           reg_fence16(sv[0]);
@@ -518,7 +528,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             if (c < 3)
               tmem_ld16x256b_x4x2_async(taddr(c + 1, kColS + 64 * hf), taddr(c + 1, kColDP + 64 * hf),
                                         sv[cur ^ 1], pv[cur ^ 1]);
-            if (grp == 0) {
+            if (grp == 0 && kb > 0) {  // second half of the constants
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 a4[k] = ld[4 * (kb + k)];
