@@ -9,7 +9,10 @@
 //
 //   split kernel    one CTA per (split, kv head, sequence) takes the G query
 //                   heads of its kv head together. 128-key chunks of K and V
-//                   come in by TMA (one copy per cache block, kStages deep).
+//                   come in by TMA (one copy per cache block), S = 3 chunks
+//                   deep, or S = 1 when every split has at most two chunks
+//                   (a short window): 44 KB of shared memory then lets four
+//                   CTAs share an SM, so the whole grid runs in one wave.
 //                   Both contractions run on the tensor cores with the keys
 //                   on the long side, so the G heads (padded to N = 16) cost
 //                   little: S^T = K Q^T (M = 128 keys) lands in tensor memory
@@ -46,7 +49,6 @@ constexpr int kDecThreads = 128;
 constexpr int kChunk = 128;                                // keys per chunk, one per thread
 constexpr uint32_t kChunkBytes = kChunk * kHeadDim * 2;    // 16 KB of K (or V)
 constexpr int kN = 16;                                     // heads padded to the product's N
-constexpr int kStages = 3;                                 // chunks of K and V resident or in flight
 constexpr float kLazy = 8.f;                               // log2 headroom of the reference max
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -57,21 +59,23 @@ constexpr uint32_t kColO = 0;    // O^T: lanes = output dims (0..63), columns = 
 constexpr uint32_t kColS = 16;   // S^T, two buffers of 16: lanes = keys, columns = heads
 constexpr uint32_t kTmemCols = 64;
 
+template <int S>
 struct __align__(1024) DecSmem {
-  uint8_t k[kStages][kChunkBytes];  // chunk stages, rows of 128 bytes, 128-byte swizzled
-  uint8_t v[kStages][kChunkBytes];
+  uint8_t k[S][kChunkBytes];        // chunk stages, rows of 128 bytes, 128-byte swizzled
+  uint8_t v[S][kChunkBytes];
   uint8_t q[kN * 128];              // [16 heads][64 dims] bf16, 128-byte swizzled (rows >= G zero)
   uint8_t pt[2][2][kN * 128];       // P^T per buffer: [64-key block][16 heads][64 keys] bf16, swizzled
   float red[4][kN];                 // cross-warp max / sum per head
-  int blk[kStages * (kChunk / 16)]; // physical blocks of the split's first kStages chunks
-  uint64_t full[kStages];           // TMA of a chunk landed
+  int blk[S * (kChunk / 16)];       // physical blocks of the split's first S chunks
+  uint64_t full[S];                 // TMA of a chunk landed
   uint64_t s_full[2];               // S^T of a chunk ready
   uint64_t pv_done[2];              // O^T += V^T P^T of a chunk done (stage and P^T free)
   uint32_t tmem_base;
   int abort;
   int bad;
 };
-constexpr size_t kDecSmemBytes = sizeof(DecSmem) + 1024;
+template <int S>
+constexpr size_t dec_smem_bytes() { return sizeof(DecSmem<S>) + 1024; }
 
 // Key range of a sequence in 128-key chunks aligned to the sequence start
 // (the cache block size divides 128), and this split's share: splits take
@@ -107,12 +111,13 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]
       : "memory");
 }
 
-template <int G>
-__global__ void __launch_bounds__(kDecThreads, 2)
+template <int G, int S>
+__global__ void __launch_bounds__(kDecThreads, S == 1 ? 4 : 2)
 decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                     DecodeProblem p) {
+  constexpr int kStages = S;
   extern __shared__ uint8_t smem_raw[];
-  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw + align1024_pad(smem_raw));
+  DecSmem<S>& sm = *reinterpret_cast<DecSmem<S>*>(smem_raw + align1024_pad(smem_raw));
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
   const Range r = split_range(p, b, split);
@@ -259,8 +264,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
   int c = 0;
   for (; c < nlocal; ++c) {
     const int st = c % kStages, buf = c & 1, j0 = chunk_start(c);
-    const int nxt = c - 1 + kStages;  // chunk whose copies this iteration issues
-    const int pb_next = (warp == 0 && c >= 1 && nxt < nlocal) ? load_blk(nxt) : 0;
+    // chunk whose copies this iteration issues: with several stages the one
+    // that reuses chunk c - 1's stage, with one stage the next chunk
+    const int nxt = S == 1 ? c + 1 : c - 1 + kStages;
+    const int pb_next = (warp == 0 && (S == 1 || c >= 1) && nxt < nlocal) ? load_blk(nxt) : 0;
     // S^T of the next chunk as early as its K tile is in
     if (warp == 0 && n_s == c + 1 && c + 1 < nlocal) {
       const int s1 = (c + 1) % kStages;
@@ -344,16 +351,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
     if (warp == 0) {
       tc_fence_after();
       issue_pv(c);
+      if constexpr (S == 1) {  // the only stage is free once this chunk's product is done
+        if (nxt < nlocal && mbar_wait_warp(&sm.pv_done[c & 1], (c >> 1) & 1, g)) {
+          issue_tma(nxt, pb_next);
+          ++n_tma;
+        }
+      }
       if (n_s == c + 1 && c + 1 < nlocal) {  // the next K tile was late
         if (mbar_wait_warp(&sm.full[(c + 1) % kStages], ((c + 1) / kStages) & 1, g)) {
           issue_s(c + 1);
           ++n_s;
         }
       }
-      if (c >= 1 && nxt < nlocal) {  // chunk c - 1's stage is free once its product is done
-        if (mbar_wait_warp(&sm.pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, g)) {
-          issue_tma(nxt, pb_next);
-          ++n_tma;
+      if constexpr (S > 1) {
+        if (c >= 1 && nxt < nlocal) {  // chunk c - 1's stage is free once its product is done
+          if (mbar_wait_warp(&sm.pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, g)) {
+            issue_tma(nxt, pb_next);
+            ++n_tma;
+          }
         }
       }
     }
@@ -454,16 +469,23 @@ __global__ void __launch_bounds__(32) decode_combine_kernel(DecodeProblem p) {
   if (p.lse && lane == 0) p.lse[(int64_t)h * p.nseq + b] = Z > 0.f ? (msub + __log2f(Z)) * kLn2 : -INFINITY;
 }
 
+template <int G, int S>
+cudaError_t launch_split_s(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeProblem& p,
+                           cudaStream_t s) {
+  constexpr size_t bytes = dec_smem_bytes<S>();
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)bytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.nsplit, p.Hkv, p.nseq);
+  decode_split_kernel<G, S><<<grid, kDecThreads, bytes, s>>>(mk, mv, p);
+  note_launch();
+  return cudaGetLastError();
+}
+
 template <int G>
 cudaError_t launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeProblem& p,
                          cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kDecSmemBytes);
-  if (e != cudaSuccess) return e;
-  const dim3 grid(p.nsplit, p.Hkv, p.nseq);
-  decode_split_kernel<G><<<grid, kDecThreads, kDecSmemBytes, s>>>(mk, mv, p);
-  note_launch();
-  return cudaGetLastError();
+  return p.split_chunks <= 2 ? launch_split_s<G, 1>(mk, mv, p, s) : launch_split_s<G, 3>(mk, mv, p, s);
 }
 
 }  // namespace
