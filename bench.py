@@ -35,6 +35,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+# numpy's BLAS runs the decode oracle's products on one thread, so the CPU
+# baseline's core count is known (the fwd/bwd oracle sets its own threads)
+for _var in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+    os.environ.setdefault(_var, "1")
 
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
