@@ -358,20 +358,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           m = m_new;
         }
         const float msub = m == -INFINITY ? 0.f : m;
-        float sum0 = 0.f, sum1 = 0.f;
+        uint64_t sumv = f2pack(0.f, 0.f);  // (even, odd) columns, two lanes per instruction
         uint32_t pa[32], pb[32];
 #pragma unroll
         for (int c = 0; c < kTile / 2; ++c) {
-          const float p0 = ex2(fmaf(s[2 * c], sl2, -msub));
-          const float p1 = ex2(fmaf(s[2 * c + 1], sl2, -msub));
-          sum0 += p0;
-          sum1 += p1;
+          const float2 x = f2unpack(ffma2(f2pack(s[2 * c], s[2 * c + 1]), f2pack(sl2, sl2), f2pack(-msub, -msub)));
+          const float p0 = ex2(x.x);
+          const float p1 = ex2(x.y);
+          sumv = fadd2(sumv, f2pack(p0, p1));
           if (c < 32)
             pa[c] = pack_bf16(p0, p1);
           else
             pb[c - 32] = pack_bf16(p0, p1);
         }
-        l += sum0 + sum1;
+        {
+          const float2 sv2 = f2unpack(sumv);
+          l += sv2.x + sv2.y;
+        }
         if (jj > 0) {
           // PV(jj-1) must be complete: it reads P and accumulates into O
           if (!mbar_wait_warp(&sm.o_done, nod & 1, g)) {
