@@ -37,6 +37,15 @@ sinkattn_status device_info(int32_t** err, int* sms) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(SINKATTN_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(SINKATTN_ERR_UNSUPPORTED, "device index out of range");
+  // make the device's context current on this host thread before anything
+  // else (tensor maps are encoded through the driver before the first launch,
+  // e.g. on a thread that has made no CUDA call yet)
+  static thread_local int bound_dev = -1;
+  if (bound_dev != dev) {
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return fail(SINKATTN_ERR_CUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
+    bound_dev = dev;
+  }
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   if (!g_err_ptr[dev]) {
     void* ptr = nullptr;
@@ -249,10 +258,13 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
   char* ws = static_cast<char*>(a->workspace);
   TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
               l.capacity};
-  cudaError_t e = launch_build_tile_list(p, 0, qt, s);
+  FwdLaunch fl;
+  cudaError_t e = prepare_fwd(p, &fl);
+  if (e != cudaSuccess) return cuda_fail(e, "forward tensor maps");
+  e = launch_build_tile_list(p, 0, qt, s);
   if (e != cudaSuccess) return cuda_fail(e, "tile list");
   record(a->timing_events[0], s);
-  e = launch_fwd(p, qt, sms, s);
+  e = launch_fwd(p, fl, qt, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "forward kernel");
   record(a->timing_events[1], s);
   return SINKATTN_OK;
@@ -299,12 +311,15 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.part_stride = l.capacity;
   TileList kt{reinterpret_cast<int32_t*>(ws + l.k_meta), reinterpret_cast<int2*>(ws + l.k_items),
               l.capacity};
-  cudaError_t e = launch_build_tile_list(bp.f, 1, kt, s);
+  BwdLaunch bl;
+  cudaError_t e = prepare_bwd_main(bp, &bl);
+  if (e != cudaSuccess) return cuda_fail(e, "backward tensor maps");
+  e = launch_build_tile_list(bp.f, 1, kt, s);
   if (e != cudaSuccess) return cuda_fail(e, "key-tile list");
   e = launch_bwd_preprocess(bp, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess");
   record(a->timing_events[0], s);
-  e = launch_bwd_main(bp, kt, sms, s);
+  e = launch_bwd_main(bp, bl, kt, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward main");
   record(a->timing_events[1], s);
   e = launch_bwd_finish(bp, kt, sms, s);

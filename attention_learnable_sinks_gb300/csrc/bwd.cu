@@ -759,23 +759,23 @@ cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(const BwdProblem& p, const TileList& ktiles, int num_sms,
-                            cudaStream_t s) {
-  CUtensorMap mq, mk, mv, mdo, mdq;
-  cudaError_t e = make_tmap_bf16_rows(&mq, p.f.q, p.f.Hq, p.f.total, p.f.q_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mk, p.f.k, p.f.Hkv, p.f.total, p.f.k_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mv, p.f.v, p.f.Hkv, p.f.total, p.f.v_stride);
+cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l) {
+  cudaError_t e = make_tmap_bf16_rows(&l->q, p.f.q, p.f.Hq, p.f.total, p.f.q_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.f.k, p.f.Hkv, p.f.total, p.f.k_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.f.v, p.f.Hkv, p.f.total, p.f.v_stride);
   if (e == cudaSuccess)
-    e = make_tmap_bf16_rows(&mdo, p.dout, p.f.Hq, p.f.total, (int64_t)p.f.Hq * kHeadDim);
-  if (e == cudaSuccess) e = make_tmap_f32_rows(&mdq, p.dq_acc, p.f.Hq, p.f.total);
+    e = make_tmap_bf16_rows(&l->dout, p.dout, p.f.Hq, p.f.total, (int64_t)p.f.Hq * kHeadDim);
+  if (e == cudaSuccess) e = make_tmap_f32_rows(&l->dq, p.dq_acc, p.f.Hq, p.f.total);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+cudaError_t launch_bwd_main(const BwdProblem& p, const BwdLaunch& l, const TileList& ktiles,
+                            int num_sms, cudaStream_t s) {
   const int64_t work = (int64_t)ktiles.capacity * p.f.Hkv;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms);
   if (grid <= 0) return cudaSuccess;
-  bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mdo, mdq, p, ktiles.items,
+  bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, l.dout, l.dq, p, ktiles.items,
                                                 ktiles.meta);
   note_launch();
   return cudaGetLastError();

@@ -448,19 +448,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 }  // namespace
 
-cudaError_t launch_fwd(const Problem& p, const TileList& qtiles, int num_sms, cudaStream_t s) {
-  CUtensorMap mq, mk, mv;
-  cudaError_t e = make_tmap_bf16_rows(&mq, p.q, p.Hq, p.total, p.q_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mk, p.k, p.Hkv, p.total, p.k_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&mv, p.v, p.Hkv, p.total, p.v_stride);
+cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l) {
+  cudaError_t e = make_tmap_bf16_rows(&l->q, p.q, p.Hq, p.total, p.q_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.k, p.Hkv, p.total, p.k_stride);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.v, p.Hkv, p.total, p.v_stride);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qtiles, int num_sms,
+                       cudaStream_t s) {
   const int64_t work = (int64_t)qtiles.capacity * p.Hq;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * 2);
   if (grid <= 0) return cudaSuccess;
-  fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p, qtiles.items, qtiles.meta);
+  fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, p, qtiles.items, qtiles.meta);
   note_launch();
   return cudaGetLastError();
 }

@@ -106,10 +106,22 @@ cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int tota
 // Launchers (each returns the cudaGetLastError() of its launch).
 cudaError_t launch_build_tile_list(const Problem& p, int by_keys, const TileList& list,
                                    cudaStream_t s);
-cudaError_t launch_fwd(const Problem& p, const TileList& qtiles, int num_sms, cudaStream_t s);
+// Tensor maps and kernel attributes are prepared before a call's first
+// launch, so that its kernels go out back to back (host-side preparation
+// between two launches would leave the GPU idle).
+struct FwdLaunch {
+  CUtensorMap q, k, v;
+};
+struct BwdLaunch {
+  CUtensorMap q, k, v, dout, dq;
+};
+cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l);
+cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l);
+cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qtiles, int num_sms,
+                       cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s);
-cudaError_t launch_bwd_main(const BwdProblem& p, const TileList& ktiles, int num_sms,
-                            cudaStream_t s);
+cudaError_t launch_bwd_main(const BwdProblem& p, const BwdLaunch& l, const TileList& ktiles,
+                            int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int num_sms,
                               cudaStream_t s);
 
