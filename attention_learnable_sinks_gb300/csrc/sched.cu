@@ -40,15 +40,17 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
   if (tid == 0) bad = (nseq >= 0 && (cu[0] != 0 || cu[nseq] != total)) ? 1 : 0;
   __syncthreads();
 
-  // pass 1: validate lengths, histogram of costs
-  for (int b = tid; b < nseq; b += kThreads) {
+  // pass 1: validate lengths, histogram of costs; a warp per sequence, its
+  // lanes over the sequence's tiles
+  const int lane = tid & 31, warp = tid >> 5;
+  for (int b = warp; b < nseq; b += kThreads / 32) {
     const int L = cu[b + 1] - cu[b];
     if (L < 0 || L > max_seqlen) {
-      atomicOr(&bad, 1);
+      if (lane == 0) atomicOr(&bad, 1);
       continue;
     }
     const int nt = (L + kTile - 1) / kTile;
-    for (int t = 0; t < nt; ++t)
+    for (int t = lane; t < nt; t += 32)
       atomicAdd(&hist[min(tile_cost(by_keys, causal, window, L, t), kBuckets - 1)], 1);
   }
   __syncthreads();
@@ -71,7 +73,6 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
     local[e] = hist[kBuckets - 1 - (tid * kPer + e)];
     sum += local[e];
   }
-  const int lane = tid & 31, warp = tid >> 5;
   int incl = sum;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -110,10 +111,10 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
   }
 
   // pass 2: scatter items into their buckets (order inside a bucket is free)
-  for (int b = tid; b < nseq; b += kThreads) {
+  for (int b = warp; b < nseq; b += kThreads / 32) {
     const int L = cu[b + 1] - cu[b];
     const int nt = (L + kTile - 1) / kTile;
-    for (int t = 0; t < nt; ++t) {
+    for (int t = lane; t < nt; t += 32) {
       const int c = min(tile_cost(by_keys, causal, window, L, t), kBuckets - 1);
       const int pos = atomicAdd(&hist[c], 1);
       items[pos] = make_int2(b, t);
