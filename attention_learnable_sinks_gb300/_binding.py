@@ -42,6 +42,8 @@ class BwdParams(ctypes.Structure):
         ("workspace", _c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("timing_events", _c_void_p * 2),
         ("accumulate_dsinks", ctypes.c_int32),
+        ("deterministic", ctypes.c_int32),
+        ("timing_events_dq", _c_void_p * 2),
     ]
 
 

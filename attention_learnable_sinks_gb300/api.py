@@ -92,10 +92,14 @@ def forward(q, k, v, sinks, cu_seqlens, max_seqlen, *, causal=True, window=0, sc
 
 def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=True, window=0,
              scale=None, dq=None, dk=None, dv=None, dsinks=None, workspace=None,
-             timing_events=None, accumulate_dsinks=False):
+             timing_events=None, accumulate_dsinks=False, deterministic=False,
+             timing_events_dq=None):
     """dq, dk, dv (bf16, shaped like q, k, v but contiguous) and dsinks [Hq]
     fp32 (None when ``sinks`` is None). With ``accumulate_dsinks`` the sink
-    gradient is added to the given ``dsinks`` instead of overwriting it."""
+    gradient is added to the given ``dsinks`` instead of overwriting it. With
+    ``deterministic`` dq is summed in a fixed order by a second,
+    query-stationary pass, so every output is bit-identical from run to run;
+    ``timing_events_dq`` (two CUDA events) are recorded around that pass."""
     _validate_inputs(q, k, v, sinks, cu_seqlens)
     for name, t in (("o", o), ("dout", dout)):
         _check_tokens(name, t, 1)
@@ -122,6 +126,8 @@ def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=Tru
     if accumulate_dsinks and dsinks is None:
         raise ValueError("accumulate_dsinks needs a dsinks tensor to add to")
     p.accumulate_dsinks = 1 if accumulate_dsinks else 0
+    p.deterministic = 1 if deterministic else 0
+    p.timing_events_dq[0], p.timing_events_dq[1] = _events(timing_events_dq)
     check(L.sinkattn_bwd(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_bwd")
     return dq, dk, dv, dsinks
 
@@ -179,30 +185,32 @@ def workspace_bytes(kind: str, nseq: int, total: int, Hq: int, Hkv: int) -> int:
 
 class _SinkAttention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale):
+    def forward(ctx, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale, deterministic):
         o, lse = forward(q, k, v, sinks, cu_seqlens, max_seqlen, causal=causal, window=window,
                          scale=scale)
         ctx.save_for_backward(q, k, v, sinks, cu_seqlens, o, lse)
-        ctx.args = (max_seqlen, causal, window, scale)
+        ctx.args = (max_seqlen, causal, window, scale, deterministic)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, sinks, cu_seqlens, o, lse = ctx.saved_tensors
-        max_seqlen, causal, window, scale = ctx.args
+        max_seqlen, causal, window, scale, deterministic = ctx.args
         dq, dk, dv, ds = backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse,
-                                  do.contiguous(), causal=causal, window=window, scale=scale)
-        return dq, dk, dv, ds, None, None, None, None, None
+                                  do.contiguous(), causal=causal, window=window, scale=scale,
+                                  deterministic=deterministic)
+        return dq, dk, dv, ds, None, None, None, None, None, None
 
 
 def sink_attention(q, k, v, sinks=None, cu_seqlens=None, max_seqlen=None, *, causal=True,
-                   window=0, scale=None):
+                   window=0, scale=None, deterministic=False):
     """Attention with one learnable sink logit per query head.
 
     q [total, Hq, 64], k/v [total, Hkv, 64] bf16 with cu_seqlens (int32
     [nseq+1]) for packed variable-length batches, or q [B, T, Hq, 64],
     k/v [B, T, Hkv, 64] for a dense batch. sinks: fp32 [Hq] or None.
-    Returns O shaped like q. Differentiable in q, k, v and sinks.
+    Returns O shaped like q. Differentiable in q, k, v and sinks; with
+    ``deterministic`` the backward is bit-identical from run to run.
     """
     batched = q.dim() == 4
     if batched:
@@ -217,7 +225,8 @@ def sink_attention(q, k, v, sinks=None, cu_seqlens=None, max_seqlen=None, *, cau
     if max_seqlen is None:
         lens = cu_seqlens[1:] - cu_seqlens[:-1]
         max_seqlen = int(lens.max().item()) if lens.numel() else 0
-    o = _SinkAttention.apply(q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale)
+    o = _SinkAttention.apply(q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale,
+                             deterministic)
     return o.reshape(B, T, *o.shape[1:]) if batched else o
 
 
@@ -252,16 +261,18 @@ class HostPipeline:
     accumulated over the groups by the backward itself. Results equal one
     ``forward`` + ``backward`` over the whole batch (dS_h up to the order of
     its float additions). Device buffers, workspaces and streams are made
-    once, for one batch shape (``cu_seqlens``, heads).
+    once, for one batch shape (``cu_seqlens``, heads). ``deterministic``
+    selects the backward whose dq is summed in a fixed order.
     """
 
     def __init__(self, cu_seqlens, Hq: int, Hkv: int, *, causal=True, window=0, scale=None,
-                 groups: int = 2, device=None):
+                 groups: int = 2, device=None, deterministic=False):
         device = torch.device(device if device is not None else "cuda")
         cu = [int(x) for x in cu_seqlens.tolist()]
         lens = [b - a for a, b in zip(cu[:-1], cu[1:])]
         self.bounds = _split_sequences(lens, causal, window, groups)
         self.causal, self.window, self.scale = causal, window, scale
+        self.deterministic = deterministic
         self.Hq, self.Hkv, self.total = Hq, Hkv, cu[-1]
         self.device = device
         d = HEAD_DIM
@@ -337,7 +348,8 @@ class HostPipeline:
                 backward(q, k, v, self.sinks, g["cu"], g["max_seqlen"], o, g["lse"], do,
                          causal=self.causal, window=self.window, scale=self.scale,
                          dq=self.dq[sl], dk=self.dk[sl], dv=self.dv[sl], dsinks=self.dsinks,
-                         workspace=self.ws_b, accumulate_dsinks=i > 0)
+                         workspace=self.ws_b, accumulate_dsinks=i > 0,
+                         deterministic=self.deterministic)
                 g["bwd"].record(self.s_run)
         # outputs: a group's o as soon as its forward is done, then its gradients
         self.s_out.wait_stream(cur)

@@ -74,7 +74,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Workspace layout. Forward: [meta | q-tile items]. Backward:
-// [meta | k-tile items | D | sink partials | dq_acc].
+// [meta | k-tile items | D | sink partials | dq_acc | meta | q-tile items]
+// (the query-tile list serves the deterministic dq pass).
 struct Layout {
   size_t q_meta, q_items, k_meta, k_items, D, part, dq_acc, bytes;
   int32_t capacity, nchunks;
@@ -101,6 +102,10 @@ Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
     off += align256(sizeof(float) * 8 * (size_t)Hq * l.capacity);
     l.dq_acc = off;
     off += align256(sizeof(float) * (size_t)total * Hq * kHeadDim);
+    l.q_meta = off;
+    off += 256;
+    l.q_items = off;
+    off += align256(sizeof(int2) * (size_t)l.capacity);
   }
   l.bytes = off;
   return l;
@@ -304,6 +309,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.dv = static_cast<__nv_bfloat16*>(a->dv);
   bp.dsinks = a->dsinks;
   bp.accumulate_dsinks = a->accumulate_dsinks != 0;
+  bp.deterministic = a->deterministic != 0;
   bp.D = reinterpret_cast<float*>(ws + l.D);
   bp.sink_part = reinterpret_cast<float*>(ws + l.part);
   bp.dq_acc = reinterpret_cast<float*>(ws + l.dq_acc);
@@ -311,17 +317,30 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.part_stride = l.capacity;
   TileList kt{reinterpret_cast<int32_t*>(ws + l.k_meta), reinterpret_cast<int2*>(ws + l.k_items),
               l.capacity};
+  TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
+              l.capacity};
   BwdLaunch bl;
   cudaError_t e = prepare_bwd_main(bp, &bl);
+  if (e == cudaSuccess && bp.deterministic) e = prepare_bwd_dq();
   if (e != cudaSuccess) return cuda_fail(e, "backward tensor maps");
   e = launch_build_tile_list(bp.f, 1, kt, s);
   if (e != cudaSuccess) return cuda_fail(e, "key-tile list");
+  if (bp.deterministic) {
+    e = launch_build_tile_list(bp.f, 0, qt, s);
+    if (e != cudaSuccess) return cuda_fail(e, "query-tile list");
+  }
   e = launch_bwd_preprocess(bp, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess");
   record(a->timing_events[0], s);
   e = launch_bwd_main(bp, bl, kt, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward main");
   record(a->timing_events[1], s);
+  if (bp.deterministic) {
+    record(a->timing_events_dq[0], s);
+    e = launch_bwd_dq(bp, bl, qt, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "deterministic dq");
+    record(a->timing_events_dq[1], s);
+  }
   e = launch_bwd_finish(bp, kt, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "dq conversion / sink gradient");
   return SINKATTN_OK;

@@ -83,9 +83,11 @@ preprocess_kernel(BwdProblem bp) {
       const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(b2[e]);
       D = fmaf(x.x, y.x, fmaf(x.y, y.y, D));
     }
-    float4* acc = reinterpret_cast<float4*>(bp.dq_acc + row * kHeadDim) + sub * 2;
-    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!bp.deterministic) {  // the atomic dq path sums into the accumulator
+      float4* acc = reinterpret_cast<float4*>(bp.dq_acc + row * kHeadDim) + sub * 2;
+      acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   D += __shfl_xor_sync(0xffffffffu, D, 1);
   D += __shfl_xor_sync(0xffffffffu, D, 2);
@@ -187,6 +189,9 @@ __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// kDQ = false: the deterministic mode's instantiation, without the dQ
+// products and read-out (dq then comes from the query-stationary pass).
+template <bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -235,7 +240,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     tma_prefetch(&tm_k);
     tma_prefetch(&tm_v);
     tma_prefetch(&tm_do);
-    tma_prefetch(&tm_dq);
+    if (kDQ) tma_prefetch(&tm_dq);
   }
   __syncthreads();
   tc_fence_after();
@@ -427,17 +432,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           if (hf == 1) umma_commit_warp(&sm.q_empty[st]);  // last reader of Q / dO
         }
         if (!ok) break;
-        if (!mbar_wait_warp(&sm.dq_empty, (ndq & 1) ^ 1, g)) {
-          ok = false;
-          break;
-        }
-        ++ndq;
-        tc_fence_after();
+        if constexpr (kDQ) {
+          if (!mbar_wait_warp(&sm.dq_empty, (ndq & 1) ^ 1, g)) {
+            ok = false;
+            break;
+          }
+          ++ndq;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time (+2048 B)
-          umma_ss_warp(tmem + kColDQ, dSm0 + db * kDsStep + 128 * k, dKmn + 128 * k, idQ, k > 0);
-        umma_commit_warp(&sm.ds_free[db]);
-        umma_commit_warp(&sm.dq_full);
+          for (int k = 0; k < kTile / 16; ++k)  // 128 keys, 16 at a time (+2048 B)
+            umma_ss_warp(tmem + kColDQ, dSm0 + db * kDsStep + 128 * k, dKmn + 128 * k, idQ, k > 0);
+          umma_commit_warp(&sm.ds_free[db]);
+          umma_commit_warp(&sm.dq_full);
+        } else {
+          umma_commit_warp(&sm.ds_free[db]);  // dK of both halves has read dS^T
+        }
         if (more && deferred) {
           if (!mbar_wait_warp(&sm.q_full[(tile + 1) % kQStages], ((tile + 1) / kQStages) & 1, g) ||
               !issue_sdp(tile + 1)) {
@@ -649,6 +658,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
       }
     }
+  } else if (warp >= 12 && !kDQ) {
+    // no dQ: these warps only keep the scheduler ring moving
+    uint32_t nsched = 0;
+    while (next_unit(sm, nsched, g, lane == 0, 0xffffffffu) >= 0) {
+    }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ read-out
     const int quarter = warp & 3;
@@ -737,7 +751,7 @@ finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
   }
   const int64_t n8 = (int64_t)p.total * p.Hq * kHeadDim / 8;
   const int64_t e = (int64_t)blockIdx.x * kFinishThreads + threadIdx.x;  // 8 elements each
-  if (e < n8) {
+  if (!bp.deterministic && e < n8) {
     const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
     const float4 a = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e];
     const float4 b = reinterpret_cast<const float4*>(bp.dq_acc)[2 * e + 1];
@@ -767,7 +781,8 @@ cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l) {
     e = make_tmap_bf16_rows(&l->dout, p.dout, p.f.Hq, p.f.total, (int64_t)p.f.Hq * kHeadDim);
   if (e == cudaSuccess) e = make_tmap_f32_rows(&l->dq, p.dq_acc, p.f.Hq, p.f.total);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  return cudaFuncSetAttribute(p.deterministic ? bwd_kernel<false> : bwd_kernel<true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
 }
 
 cudaError_t launch_bwd_main(const BwdProblem& p, const BwdLaunch& l, const TileList& ktiles,
@@ -775,8 +790,12 @@ cudaError_t launch_bwd_main(const BwdProblem& p, const BwdLaunch& l, const TileL
   const int64_t work = (int64_t)ktiles.capacity * p.f.Hkv;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms);
   if (grid <= 0) return cudaSuccess;
-  bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, l.dout, l.dq, p, ktiles.items,
-                                                ktiles.meta);
+  if (p.deterministic)
+    bwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, l.dout, l.dq, p, ktiles.items,
+                                                         ktiles.meta);
+  else
+    bwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, l.dout, l.dq, p, ktiles.items,
+                                                        ktiles.meta);
   note_launch();
   return cudaGetLastError();
 }
@@ -786,7 +805,8 @@ cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int n
   (void)num_sms;
   const int64_t n8 = (int64_t)p.f.total * p.f.Hq * kHeadDim / 8;
   const int64_t head_blocks = (p.f.Hq + kFinishThreads / 32 - 1) / (kFinishThreads / 32);
-  const int64_t blocks = std::max<int64_t>(head_blocks, (n8 + kFinishThreads - 1) / kFinishThreads);
+  const int64_t blocks =
+      p.deterministic ? head_blocks : std::max<int64_t>(head_blocks, (n8 + kFinishThreads - 1) / kFinishThreads);
   finish_kernel<<<(unsigned)blocks, kFinishThreads, 0, s>>>(p, ktiles.meta);
   note_launch();
   return cudaGetLastError();

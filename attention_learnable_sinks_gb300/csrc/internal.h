@@ -43,6 +43,7 @@ struct BwdProblem {
   int32_t nchunks;             // token chunks of the preprocess pass
   int32_t part_stride;         // key-tile capacity
   int32_t accumulate_dsinks;   // add to dsinks instead of overwriting it
+  int32_t deterministic;       // dq from the query-stationary pass (no dq_acc)
 };
 
 // Decode over a paged KV cache, as the kernels see it.
@@ -124,6 +125,11 @@ cudaError_t launch_bwd_main(const BwdProblem& p, const BwdLaunch& l, const TileL
                             int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int num_sms,
                               cudaStream_t s);
+// Deterministic dq: query-stationary pass over the query-tile list, on the
+// main kernel's Q / K / V / dO tensor maps.
+cudaError_t prepare_bwd_dq();
+cudaError_t launch_bwd_dq(const BwdProblem& p, const BwdLaunch& l, const TileList& qtiles,
+                          int num_sms, cudaStream_t s);
 
 size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit);
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t s);

@@ -326,9 +326,11 @@ def run_gb300(args):
         return evs
 
     K = args.steps
+    det = args.deterministic
     step_ev = [new_events(2) for _ in range(K)]
     fwd_ev = [new_events(2) for _ in range(K)]
     bwd_ev = [new_events(2) for _ in range(K)]
+    dq_ev = [new_events(2) for _ in range(K)] if det else None
 
     def step(i=None):
         api.forward(q, k, v, s, cu, maxlen, causal=w.causal, window=w.window, scale=w.scale,
@@ -336,7 +338,8 @@ def run_gb300(args):
                     timing_events=None if i is None else fwd_ev[i])
         api.backward(q, k, v, s, cu, maxlen, o, lse, do, causal=w.causal, window=w.window,
                      scale=w.scale, dq=dq, dk=dk, dv=dv, dsinks=ds, workspace=ws_b,
-                     timing_events=None if i is None else bwd_ev[i])
+                     timing_events=None if i is None else bwd_ev[i], deterministic=det,
+                     timing_events_dq=None if i is None or not det else dq_ev[i])
 
     for _ in range(args.warmup):
         step()
@@ -365,6 +368,7 @@ def run_gb300(args):
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
     bwd_ms = [a.elapsed_time(b) for a, b in bwd_ev]
+    dq_ms = [a.elapsed_time(b) for a, b in dq_ev] if det else None
     total_ms = reduce_max(sum(step_ms), world, device)
     ms_per_step = total_ms / K
     value = flops * world * K / (total_ms / 1e3) / 1e12
@@ -380,7 +384,8 @@ def run_gb300(args):
     hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
     hds = torch.empty(ds.shape, dtype=ds.dtype).pin_memory()
     pipe = api.HostPipeline(w.cu_seqlens, w.Hq, w.Hkv, causal=w.causal, window=w.window,
-                            scale=w.scale, groups=args.e2e_groups, device=device)
+                            scale=w.scale, groups=args.e2e_groups, device=device,
+                            deterministic=det)
     h2d, d2h = pipe.h2d_bytes(), pipe.d2h_bytes()
 
     def e2e_step():
@@ -406,10 +411,16 @@ def run_gb300(args):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     f_avg, b_avg = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    if b_avg >= f_avg:
-        dom, dom_ms, dom_flops, dom_file = "bwd main", b_avg, bwd_flops, "bwd.cu"
-    else:
-        dom, dom_ms, dom_flops, dom_file = "fwd", f_avg, fwd_flops, "fwd.cu"
+    q_avg = statistics.mean(dq_ms) if det else None
+    # the deterministic dq pass recomputes S and dP and forms dQ: three
+    # products where the forward has two; in that mode the main backward's
+    # algorithmic work is its dk / dv products (S, dP, dV, dK: 4 of 5)
+    dq_flops = 1.5 * fwd_flops
+    main_flops = 0.8 * bwd_flops if det else bwd_flops
+    cands = [("fwd", f_avg, fwd_flops, "fwd.cu"), ("bwd main", b_avg, main_flops, "bwd.cu")]
+    if det:
+        cands.append(("dq pass", q_avg, dq_flops, "dq.cu"))
+    dom, dom_ms, dom_flops, dom_file = max(cands, key=lambda c: c[1])
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     tr = traffic_record(dom_file) if args.workload == "dense" else None
     if w.window > 0:
@@ -418,10 +429,12 @@ def run_gb300(args):
         # Algorithmic bytes per launch, per token (d = 64):
         #   forward:       read q, k, v; write o, LSE
         #   backward main: read q, dO, k, v, LSE, D; write dk, dv and the fp32
-        #                  dq accumulator once
+        #                  dq accumulator once (no accumulator when deterministic)
+        #   dq pass:       read q, dO, k, v, LSE, D; write dq
         d, Hq, Hkv = 64, w.Hq, w.Hkv
-        per_tok = (2 * Hq * d + 4 * Hkv * d + 2 * Hq * d + 4 * Hq) if dom == "fwd" else \
-            (4 * Hq * d + 4 * Hkv * d + 8 * Hq + 4 * Hkv * d + 4 * Hq * d)
+        per_tok = {"fwd": 2 * Hq * d + 4 * Hkv * d + 2 * Hq * d + 4 * Hq,
+                   "bwd main": 4 * Hq * d + 4 * Hkv * d + 8 * Hq + 4 * Hkv * d + (0 if det else 4 * Hq * d),
+                   "dq pass": 4 * Hq * d + 4 * Hkv * d + 8 * Hq + 2 * Hq * d}[dom]
         gbs = per_tok * w.total / (dom_ms / 1e3) / 1e9
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roofline = {"bound": "hbm", "kernel": dom, "achieved": gbs, "peak": hbm, "unit": "GB/s",
@@ -449,13 +462,18 @@ def run_gb300(args):
         "frac_of_nominal_peak": (value / world / nominal) if nominal else None,
         "fwd_ms": f_avg, "bwd_main_ms": b_avg,
         "fwd_tflops": fwd_flops / (f_avg / 1e3) / 1e12,
-        "bwd_main_tflops": bwd_flops / (b_avg / 1e3) / 1e12,
+        "bwd_main_tflops": main_flops / (b_avg / 1e3) / 1e12,
+        "deterministic_backward": det,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K},
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if det:
+        line["dq_pass_ms"] = q_avg
+        line["dq_pass_tflops"] = dq_flops / (q_avg / 1e3) / 1e12
+        line["config"]["backward"] = "deterministic: dq from a fixed-order query-stationary pass"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, f = oracle_sample_run(w, **ORACLE_SAMPLE)
         import oracle
@@ -664,6 +682,8 @@ def main(argv=None):
                     choices=("tiny", "dense", "window", "varlen", "long", "long_window",
                              "decode", "decode_window"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="backward with dq summed in a fixed order (query-stationary dq pass)")
     ap.add_argument("--e2e-groups", type=int, default=2,
                     help="groups of whole sequences streamed by the end-to-end leg")
     args = ap.parse_args(argv)

@@ -127,6 +127,16 @@ typedef struct sinkattn_bwd_params {
                                   dL/dS_h (gradient accumulation over several
                                   calls, e.g. micro-batches or groups of
                                   sequences of one batch)                     */
+  int32_t deterministic;       /* 0: dq is summed over key tiles with atomic
+                                  adds (fastest; the order of the sum, and so
+                                  the last bits of dq, can change from run to
+                                  run). Nonzero: dq comes from a second,
+                                  query-stationary pass that sums the key
+                                  tiles of each query tile in a fixed order,
+                                  so every output is bit-identical from run to
+                                  run (dk, dv and dsinks always are).        */
+  void* timing_events_dq[2];   /* optional, around the deterministic dq pass
+                                  (ignored when deterministic = 0)           */
 } sinkattn_bwd_params;
 
 /* Workspace sizes in bytes for a problem of this shape (0 on bad input). */

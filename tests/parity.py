@@ -27,8 +27,9 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def run_cuda(w: Workload, device="cuda", q_view=None, k_view=None, v_view=None, scale=None,
-             sinks=True):
-    """One forward + backward through the C ABI; returns fp64 host arrays."""
+             sinks=True, deterministic=False):
+    """One forward + backward through the C ABI; returns fp64 host arrays.
+    ``deterministic`` selects the backward whose dq is summed in a fixed order."""
     q = q_view if q_view is not None else w.q.to(device)
     k = k_view if k_view is not None else w.k.to(device)
     v = v_view if v_view is not None else w.v.to(device)
@@ -39,7 +40,8 @@ def run_cuda(w: Workload, device="cuda", q_view=None, k_view=None, v_view=None, 
     o, lse = api.forward(q, k, v, s, cu, max(w.max_seqlen, 1), causal=w.causal, window=w.window,
                          scale=sc)
     dq, dk, dv, ds = api.backward(q, k, v, s, cu, max(w.max_seqlen, 1), o, lse, do,
-                                  causal=w.causal, window=w.window, scale=sc)
+                                  causal=w.causal, window=w.window, scale=sc,
+                                  deterministic=deterministic)
     torch.cuda.synchronize()
     err = _binding.device_error(reset=True)
     assert err == 0, f"device error word {err}"

@@ -34,29 +34,32 @@ SMALL = [
 def test_small_cases_match_oracle(cuda_lib, case):
     name, lengths, Hq, Hkv, causal, window, extra = case
     w = make(name, lengths, Hq, Hkv, seed=100 + len(name), causal=causal, window=window, **extra)
-    got = run_cuda(w)
     ref, tok, qh, kvh = run_oracle(w)
-    compare_full(w, got, ref)
     s = w.sinks.numpy().astype(np.float64)
     cond = dsink_condition(s, ref["lse"], ref["o"], ref["_do"])
-    assert_dsinks(got["dsinks"], ref["dsinks"], cond)
+    for det in (False, True):  # atomic dq, then the fixed-order dq pass
+        got = run_cuda(w, deterministic=det)
+        compare_full(w, got, ref)
+        assert_dsinks(got["dsinks"], ref["dsinks"], cond)
 
 
 def test_tiny_config_matches_oracle(cuda_lib):
     w = config("tiny")
-    got = run_cuda(w)
     ref, *_ = run_oracle(w)
-    compare_full(w, got, ref)
     cond = dsink_condition(w.sinks.numpy().astype(np.float64), ref["lse"], ref["o"], ref["_do"])
-    assert_dsinks(got["dsinks"], ref["dsinks"], cond)
+    for det in (False, True):
+        got = run_cuda(w, deterministic=det)
+        compare_full(w, got, ref)
+        assert_dsinks(got["dsinks"], ref["dsinks"], cond)
 
 
 def test_no_sink_matches_oracle(cuda_lib):
     w = make("nosink", [333, 90], 8, 2, seed=7)
-    got = run_cuda(w, sinks=False)
     ref, *_ = run_oracle(w, sinks=False)
-    compare_full(w, got, ref)
-    assert np.all(got["dsinks"] == 0)
+    for det in (False, True):
+        got = run_cuda(w, sinks=False, deterministic=det)
+        compare_full(w, got, ref)
+        assert np.all(got["dsinks"] == 0)
 
 
 def test_custom_scale(cuda_lib):
