@@ -98,9 +98,12 @@ def kernel_source_sha(kernel_file: str):
     return h.hexdigest()[:16]
 
 
-def traffic_record(kernel_file: str):
+def traffic_record(key: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, valid only while the kernel source is unchanged."""
+    summary, valid only while the kernel source is unchanged. ``key`` is the
+    kernel's source file, with "#deterministic" for the main backward's
+    deterministic-mode instantiation."""
+    kernel_file = key.split("#")[0]
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -110,7 +113,7 @@ def traffic_record(kernel_file: str):
     sha = kernel_source_sha(kernel_file)
     if sha is None:
         return None
-    entry = rec.get(kernel_file)
+    entry = rec.get(key)
     if not entry or entry.get("source_sha") != sha:
         return None
     return entry
@@ -422,7 +425,8 @@ def run_gb300(args):
         cands.append(("dq pass", q_avg, dq_flops, "dq.cu"))
     dom, dom_ms, dom_flops, dom_file = max(cands, key=lambda c: c[1])
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
-    tr = traffic_record(dom_file) if args.workload == "dense" else None
+    dom_key = dom_file + ("#deterministic" if det and dom == "bwd main" else "")
+    tr = traffic_record(dom_key) if args.workload == "dense" else None
     if w.window > 0:
         # a band of W keys: about W flop per byte moved, below the ridge
         # (1910.8 TFLOP/s / 6786.6 GB/s = 282 flop/B), so HBM bounds it.
