@@ -198,7 +198,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const uint64_t dKmn0 = sdesc_sw128(smem_u32(sm.k[0]), 8192, 1024);   // MN-major
     const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
     constexpr uint64_t kStageStep = kTileBytes >> 4;  // between stages of one array
-    uint32_t nq = 0, nkv = 0, nsdp = 0, nds = 0, nsched = 0;
+    uint32_t nq = 0, nsdp = 0, nds = 0, nsched = 0;
     bool ok = true;
     // S and dP of the key tile in K / V stage c % kKVStages (the softmax must
     // have read the previous tile's)
@@ -219,48 +219,71 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       umma_commit_warp(&sm.sdp_full);
       return true;
     };
-    while (ok) {
-      const int slot = nsched % kSchedSlots;
-      if (!mbar_wait_warp(&sm.sched_full[slot], (nsched / kSchedSlots) & 1, g)) break;
-      ++nsched;
-      const int w = __shfl_sync(0xffffffffu, sm.sched_unit[slot], 0);  // warp-uniform
-      const int n = __shfl_sync(0xffffffffu, sm.sched_u[slot].kt1 - sm.sched_u[slot].kt0, 0);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.sched_empty[slot]);
-      if (w < 0) break;
-      const uint32_t qb = nq & 1, dqb = nq & 1;
-      if (!mbar_wait_warp(&sm.q_full[qb], (nq >> 1) & 1, g) ||
-          !mbar_wait_warp(&sm.dq_empty[dqb], ((nq >> 1) & 1) ^ 1, g))
-        break;
-      ++nq;
-      if (n > 0 && !issue_sdp(qb, nkv)) break;
-      if (n <= 1) umma_commit_warp(&sm.q_empty[qb]);  // last reader of Q / dO issued
-      for (int jj = 0; jj < n; ++jj) {
-        if (jj + 1 < n) {
-          if (!issue_sdp(qb, nkv + 1)) {
-            ok = false;
-            break;
-          }
-          if (jj + 2 == n) umma_commit_warp(&sm.q_empty[qb]);
-        }
-        const int st = nkv % kKVStages, db = nds & 1;
-        if (!mbar_wait_warp(&sm.ds_full[db], (nds >> 1) & 1, g)) {
-          ok = false;
-          break;
-        }
-        ++nds;
-        tc_fence_after();
-        const uint64_t bk = dKmn0 + st * kStageStep;
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)  // dS from tensor memory; +2048 B of K per 16 keys
-          umma_ts_warp(tmem + kColDQ + 64 * dqb, tmem + kColDS + 64 * db + 8 * k, bk + 128 * k, idQ,
-                       (jj > 0 || k > 0) ? 1u : 0u);
-        umma_commit_warp(&sm.ds_free[db]);
-        umma_commit_warp(&sm.kv_empty[st]);
-        ++nkv;
+    // The units are one stream of (unit, key tile) steps: S / dP of the next
+    // step -- the next unit's first tile at the end of a unit -- are issued
+    // before dQ of the current one, so that a unit boundary leaves no gap in
+    // the tensor pipe. fetch() returns 1 with the index of the next unit that
+    // has key tiles (its Q / dO stage and dQ buffer are index % 2), 0 at the
+    // end of the work, -1 on abort.
+    auto fetch = [&](int& n, uint32_t& u) -> int {
+      for (;;) {
+        const int slot = nsched % kSchedSlots;
+        if (!mbar_wait_warp(&sm.sched_full[slot], (nsched / kSchedSlots) & 1, g)) return -1;
+        ++nsched;
+        const int w = __shfl_sync(0xffffffffu, sm.sched_unit[slot], 0);  // warp-uniform
+        n = __shfl_sync(0xffffffffu, sm.sched_u[slot].kt1 - sm.sched_u[slot].kt0, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sched_empty[slot]);
+        if (w < 0) return 0;
+        u = nq++;
+        if (!mbar_wait_warp(&sm.q_full[u & 1], (u >> 1) & 1, g)) return -1;
+        if (n > 0) return 1;
+        // no key tile: nothing reads Q / dO, and dq is written as zero
+        if (!mbar_wait_warp(&sm.dq_empty[u & 1], ((u >> 1) & 1) ^ 1, g)) return -1;
+        umma_commit_warp(&sm.q_empty[u & 1]);
+        umma_commit_warp(&sm.dq_full[u & 1]);
       }
-      if (!ok) break;
-      umma_commit_warp(&sm.dq_full[dqb]);
+    };
+    int n = 0, jj = 0;
+    uint32_t u = 0;
+    int got = fetch(n, u);
+    uint32_t c = 0;  // K / V load of the current step
+    if (got > 0) {
+      ok = issue_sdp(u & 1, c);
+      if (ok && n == 1) umma_commit_warp(&sm.q_empty[u & 1]);  // last reader of Q / dO issued
+    }
+    while (got > 0 && ok) {
+      int n2 = n, jj2 = jj + 1;
+      uint32_t u2 = u;
+      if (jj2 == n) {
+        got = fetch(n2, u2);
+        jj2 = 0;
+        if (got < 0) break;
+      }
+      if (got > 0) {
+        if (!issue_sdp(u2 & 1, c + 1)) break;
+        if (jj2 == n2 - 1) umma_commit_warp(&sm.q_empty[u2 & 1]);
+      }
+      // dQ of the current step; a unit's first one waits until the read-out
+      // of the unit that used this accumulator before
+      const uint32_t dqb = u & 1;
+      if (jj == 0 && !mbar_wait_warp(&sm.dq_empty[dqb], ((u >> 1) & 1) ^ 1, g)) break;
+      const int st = c % kKVStages, db = nds & 1;
+      if (!mbar_wait_warp(&sm.ds_full[db], (nds >> 1) & 1, g)) break;
+      ++nds;
+      tc_fence_after();
+      const uint64_t bk = dKmn0 + st * kStageStep;
+#pragma unroll
+      for (int k = 0; k < kTile / 16; ++k)  // dS from tensor memory; +2048 B of K per 16 keys
+        umma_ts_warp(tmem + kColDQ + 64 * dqb, tmem + kColDS + 64 * db + 8 * k, bk + 128 * k, idQ,
+                     (jj > 0 || k > 0) ? 1u : 0u);
+      umma_commit_warp(&sm.ds_free[db]);
+      umma_commit_warp(&sm.kv_empty[st]);
+      if (jj == n - 1) umma_commit_warp(&sm.dq_full[dqb]);
+      ++c;
+      n = n2;
+      jj = jj2;
+      u = u2;
     }
     umma_commit_warp(&sm.drain);  // every product issued above has completed
     if (lane == 0) drain_wait(&sm.drain, 0);
@@ -276,8 +299,41 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const uint64_t sl2x2 = f2pack(p.scale_log2, p.scale_log2);
     uint32_t nsdp = 0, nds = 0, nunit = 0, nsched = 0;
     bool ok = true;
+    // A unit's epilogue is deferred until this thread has formed dS of the
+    // next unit's first key tile: by then the unit's last dQ product has
+    // completed, and S / dP of the next unit were not kept waiting for it.
+    // The pending unit's ring slot stays held until its epilogue.
+    struct Pending {
+      int64_t orow;  // output row (token * Hq + head)
+      int slot;
+      bool valid, any;
+    } pend{0, 0, false, false};
+    bool has_pend = false;
+    auto epilogue = [&]() -> bool {  // dq = bf16(scale * dQ), columns 32 wg .. 32 wg + 31
+      const int dqb = nunit & 1;
+      if (!mbar_wait_warp(&sm.dq_full[dqb], (nunit >> 1) & 1, g)) return false;
+      ++nunit;
+      tc_fence_after();
+      uint32_t a[32];
+      tmem_ld32(tmem + lane_off + kColDQ + 64 * dqb + 32 * wg, a);
+      tc_fence_before();
+      mbar_arrive(&sm.dq_empty[dqb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.sched_empty[pend.slot]);  // the slot is no longer read
+      if (pend.valid) {
+        const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
+        uint32_t ob[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          ob[e] = pend.any ? pack_bf16(__uint_as_float(a[2 * e]) * sc, __uint_as_float(a[2 * e + 1]) * sc) : 0u;
+        uint4* dst = reinterpret_cast<uint4*>(bp.dq + pend.orow * kHeadDim + 32 * wg);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+      }
+      has_pend = false;
+      return true;
+    };
     while (ok) {
-      // the ring slot stays held until the epilogue has read the unit
       const int slot = nsched % kSchedSlots;
       if (!mbar_wait_warp(&sm.sched_full[slot], (nsched / kSchedSlots) & 1, g)) break;
       ++nsched;
@@ -293,12 +349,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       const uint64_t nl2x2 = f2pack(nl2, nl2), ndx2 = f2pack(nd, nd);
       const int khi = p.causal ? min(i + 1, L) : L;
       const int klo = p.window > 0 ? max(0, i - p.window + 1) : 0;
-      for (int jj = 0; jj < n; ++jj) {
+      // one key tile: S / dP in, dS out
+      auto tile = [&](int jj) -> bool {
         const int kb = (kt0 + jj) * kTile + 64 * wg;  // first key of this thread's half
-        if (!mbar_wait_warp(&sm.sdp_full, nsdp & 1, g)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait_warp(&sm.sdp_full, nsdp & 1, g)) return false;
         ++nsdp;
         tc_fence_after();
         uint32_t sv[64], pv[64];
@@ -326,41 +380,26 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           ds[c] = pack_bf16(d.x, d.y);
         }
         const int db = nds & 1;
-        if (!mbar_wait_warp(&sm.ds_free[db], ((nds >> 1) & 1) ^ 1, g)) {  // dQ of tile jj - 2 done
-          ok = false;
-          break;
-        }
+        if (!mbar_wait_warp(&sm.ds_free[db], ((nds >> 1) & 1) ^ 1, g))  // dQ of tile jj - 2 done
+          return false;
         ++nds;
         tc_fence_after();
         tmem_st32(tmem + lane_off + kColDS + 64 * db + 32 * wg, ds);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.ds_full[db]);
-      }
+        return true;
+      };
+      // the previous unit's epilogue goes after the first tile (or at once
+      // for a unit without key tiles)
+      if (n > 0) ok = tile(0);
+      if (ok && has_pend) ok = epilogue();
+      for (int jj = 1; jj < n && ok; ++jj) ok = tile(jj);
       if (!ok) break;
-      // epilogue: dq = bf16(scale * dQ), columns 32 wg .. 32 wg + 31 of this row
-      const int dqb = nunit & 1;
-      if (!mbar_wait_warp(&sm.dq_full[dqb], (nunit >> 1) & 1, g)) break;
-      ++nunit;
-      tc_fence_after();
-      uint32_t a[32];
-      tmem_ld32(tmem + lane_off + kColDQ + 64 * dqb + 32 * wg, a);
-      tc_fence_before();
-      mbar_arrive(&sm.dq_empty[dqb]);
-      const int64_t orow = (int64_t)(uv.base + i) * p.Hq + uv.h;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.sched_empty[slot]);  // the slot is no longer read
-      if (valid) {
-        const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
-        uint32_t ob[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          ob[e] = n > 0 ? pack_bf16(__uint_as_float(a[2 * e]) * sc, __uint_as_float(a[2 * e + 1]) * sc) : 0u;
-        uint4* dst = reinterpret_cast<uint4*>(bp.dq + orow * kHeadDim + 32 * wg);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-      }
+      pend = Pending{(int64_t)(uv.base + i) * p.Hq + uv.h, slot, valid, n > 0};
+      has_pend = true;
     }
+    if (ok && has_pend) epilogue();  // the last unit
   }
 
   tc_fence_before();
