@@ -244,45 +244,52 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         umma_commit_warp(&sm.dq_full[u & 1]);
       }
     };
-    int n = 0, jj = 0;
-    uint32_t u = 0;
-    int got = fetch(n, u);
-    uint32_t c = 0;  // K / V load of the current step
-    if (got > 0) {
-      ok = issue_sdp(u & 1, c);
-      if (ok && n == 1) umma_commit_warp(&sm.q_empty[u & 1]);  // last reader of Q / dO issued
-    }
-    while (got > 0 && ok) {
-      int n2 = n, jj2 = jj + 1;
-      uint32_t u2 = u;
-      if (jj2 == n) {
-        got = fetch(n2, u2);
-        jj2 = 0;
-        if (got < 0) break;
-      }
-      if (got > 0) {
-        if (!issue_sdp(u2 & 1, c + 1)) break;
-        if (jj2 == n2 - 1) umma_commit_warp(&sm.q_empty[u2 & 1]);
-      }
-      // dQ of the current step; a unit's first one waits until the read-out
-      // of the unit that used this accumulator before
-      const uint32_t dqb = u & 1;
-      if (jj == 0 && !mbar_wait_warp(&sm.dq_empty[dqb], ((u >> 1) & 1) ^ 1, g)) break;
+    // dQ of step jj of unit u (K / V load c): waits for dS, then 8 products
+    auto dq_step = [&](uint32_t u, int jj, uint32_t c) -> bool {
       const int st = c % kKVStages, db = nds & 1;
-      if (!mbar_wait_warp(&sm.ds_full[db], (nds >> 1) & 1, g)) break;
+      if (!mbar_wait_warp(&sm.ds_full[db], (nds >> 1) & 1, g)) return false;
       ++nds;
       tc_fence_after();
       const uint64_t bk = dKmn0 + st * kStageStep;
 #pragma unroll
       for (int k = 0; k < kTile / 16; ++k)  // dS from tensor memory; +2048 B of K per 16 keys
-        umma_ts_warp(tmem + kColDQ + 64 * dqb, tmem + kColDS + 64 * db + 8 * k, bk + 128 * k, idQ,
+        umma_ts_warp(tmem + kColDQ + 64 * (u & 1), tmem + kColDS + 64 * db + 8 * k, bk + 128 * k, idQ,
                      (jj > 0 || k > 0) ? 1u : 0u);
       umma_commit_warp(&sm.ds_free[db]);
       umma_commit_warp(&sm.kv_empty[st]);
-      if (jj == n - 1) umma_commit_warp(&sm.dq_full[dqb]);
+      return true;
+    };
+    int n = 0;
+    uint32_t u = 0, c = 0;  // c: K / V load of the current step
+    int got = fetch(n, u);
+    if (got > 0) {
+      ok = issue_sdp(u & 1, c);
+      if (ok && n == 1) umma_commit_warp(&sm.q_empty[u & 1]);  // last reader of Q / dO issued
+    }
+    while (got > 0 && ok) {
+      // the unit's first dQ waits until the read-out of the unit that used
+      // this accumulator before
+      if (!mbar_wait_warp(&sm.dq_empty[u & 1], ((u >> 1) & 1) ^ 1, g)) break;
+      // every step but the last: S / dP of the next tile, then dQ of this one
+      for (int jj = 0; jj + 1 < n && ok; ++jj, ++c) {
+        ok = issue_sdp(u & 1, c + 1);
+        if (ok && jj + 2 == n) umma_commit_warp(&sm.q_empty[u & 1]);
+        if (ok) ok = dq_step(u, jj, c);
+      }
+      if (!ok) break;
+      // the last step: the next unit's first S / dP go in before its dQ
+      int n2 = 0;
+      uint32_t u2 = 0;
+      got = fetch(n2, u2);
+      if (got < 0) break;
+      if (got > 0) {
+        if (!issue_sdp(u2 & 1, c + 1)) break;
+        if (n2 == 1) umma_commit_warp(&sm.q_empty[u2 & 1]);
+      }
+      if (!dq_step(u, n - 1, c)) break;
+      umma_commit_warp(&sm.dq_full[u & 1]);
       ++c;
       n = n2;
-      jj = jj2;
       u = u2;
     }
     umma_commit_warp(&sm.drain);  // every product issued above has completed
