@@ -89,6 +89,12 @@ preprocess_kernel(BwdProblem bp) {
       acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+  if (p.sinks) {  // sink partials: key tiles that do not exist stay zero
+    const int64_t np = (int64_t)p.Hq * bp.part_stride * 8;
+    for (int64_t e = (int64_t)blockIdx.x * kPrepThreads + threadIdx.x; e < np;
+         e += (int64_t)gridDim.x * kPrepThreads)
+      bp.sink_part[e] = 0.f;
+  }
   D += __shfl_xor_sync(0xffffffffu, D, 1);
   D += __shfl_xor_sync(0xffffffffu, D, 2);
   D += __shfl_xor_sync(0xffffffffu, D, 4);
@@ -128,17 +134,20 @@ struct __align__(1024) Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 struct Unit {
-  int item, base, L, c0, nkeys, kvh, qt0, nq;
+  int tidx, base, L, c0, nkeys, kvh, qt0, nq;
 };
 
 __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int w) {
   Unit u;
-  u.item = w / p.Hkv;
-  const int2 it = items[u.item];
+  const int2 it = items[w / p.Hkv];
   u.kvh = w % p.Hkv;
   u.base = p.cu[it.x];
   u.L = p.cu[it.x + 1] - u.base;
   u.c0 = it.y * kTile;
+  // a number for the key tile that does not depend on the list's order:
+  // b + (cu[b] + c0) / 128 is unique over the packing and below its tile
+  // capacity (the sink-gradient partials are stored under it)
+  u.tidx = it.x + (u.base + u.c0) / kTile;
   const int c1 = min(u.L, u.c0 + kTile);
   u.nkeys = c1 - u.c0;
   int lo, hi;
@@ -615,7 +624,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           if (lane == 0)
-            bp.sink_part[((int64_t)(u.kvh * G + hh) * bp.part_stride + u.item) * 8 + hf * 4 +
+            bp.sink_part[((int64_t)(u.kvh * G + hh) * bp.part_stride + u.tidx) * 8 + hf * 4 +
                          quarter] = v;
           sa0 = sa1 = f2pack(0.f, 0.f);
         }
@@ -719,16 +728,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 constexpr int kFinishThreads = 256;
 
 __global__ void __launch_bounds__(kFinishThreads)
-finish_kernel(BwdProblem bp, const int32_t* __restrict__ kmeta) {
+finish_kernel(BwdProblem bp) {
   const Problem& p = bp.f;
-  // dS_h: one warp per head. Lane-strided fp64 sums, then a fixed butterfly,
-  // so the result does not depend on timing.
+  // dS_h: one warp per head, over the partials in key-tile order (not list
+  // order). Lane-strided fp64 sums, then a fixed butterfly, so the result
+  // depends neither on timing nor on the work list's order.
   const int hw = blockIdx.x * (kFinishThreads / 32) + threadIdx.x / 32;
   if (bp.dsinks && hw < p.Hq) {
     const int lane = threadIdx.x & 31;
     double acc = 0.0;
     if (p.sinks) {
-      const int n = 8 * kmeta[0];
+      const int n = 8 * bp.part_stride;
       const float* part = bp.sink_part + (int64_t)hw * bp.part_stride * 8;
       for (int c = lane; c < n; c += 32) acc += (double)part[c];
     }
@@ -790,11 +800,12 @@ cudaError_t launch_bwd_main(const BwdProblem& p, const BwdLaunch& l, const TileL
 cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int num_sms,
                               cudaStream_t s) {
   (void)num_sms;
+  (void)ktiles;
   const int64_t n8 = (int64_t)p.f.total * p.f.Hq * kHeadDim / 8;
   const int64_t head_blocks = (p.f.Hq + kFinishThreads / 32 - 1) / (kFinishThreads / 32);
   const int64_t blocks =
       p.deterministic ? head_blocks : std::max<int64_t>(head_blocks, (n8 + kFinishThreads - 1) / kFinishThreads);
-  finish_kernel<<<(unsigned)blocks, kFinishThreads, 0, s>>>(p, ktiles.meta);
+  finish_kernel<<<(unsigned)blocks, kFinishThreads, 0, s>>>(p);
   note_launch();
   return cudaGetLastError();
 }

@@ -37,8 +37,9 @@ struct BwdProblem {
   __nv_bfloat16* dv;
   float* dsinks;
   float* D;                    // [Hq, total] workspace: rowsum(dO * O)
-  float* sink_part;            // [Hq, part_stride, 8] workspace: per key tile and
-                               // softmax warp, sum of p_sink * P * dP
+  float* sink_part;            // [Hq, part_stride, 8] workspace: per key tile
+                               // (numbered b + (cu[b] + c0) / 128) and softmax
+                               // warp, sum of p_sink * P * dP
   float* dq_acc;               // [total, Hq, 64] fp32 workspace
   int32_t nchunks;             // token chunks of the preprocess pass
   int32_t part_stride;         // key-tile capacity
