@@ -37,6 +37,37 @@ def test_param_struct_sizes_match():
     assert lib.sinkattn_params_size(3) == 0
 
 
+def test_param_struct_field_offsets_match(tmp_path):
+    """Every field of the binding's structs sits where the C header puts it
+    (sizes alone miss two same-sized fields in swapped order). A small C
+    program compiled against include/sinkattn.h prints the offsets."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = (("sinkattn_fwd_params", FwdParams), ("sinkattn_bwd_params", BwdParams),
+               ("sinkattn_decode_params", DecodeParams))
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "sinkattn.h"',
+             "int main(void) {"]
+    for cname, cls in structs:
+        for name, _ in cls._fields_:
+            lines.append(f'  printf("{cname}.{name} %zu\\n", offsetof({cname}, {name}));')
+        lines.append(f'  printf("{cname} %zu\\n", sizeof({cname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "offsets.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "offsets"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    got = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                        text=True).stdout.splitlines())
+    for cname, cls in structs:
+        for name, _ in cls._fields_:
+            assert int(got[f"{cname}.{name}"]) == getattr(cls, name).offset, f"{cname}.{name}"
+        assert int(got[cname]) == ctypes.sizeof(cls), cname
+
+
 def test_workspace_sizes():
     lib = _binding.lib()
     f = lib.sinkattn_fwd_workspace_size(4, 8192, 64, 8, 64)
