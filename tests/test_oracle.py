@@ -19,6 +19,7 @@ for dL/dS_h was written). So the oracle is pinned by:
 """
 
 import math
+import zlib
 
 import numpy as np
 import pytest
@@ -118,13 +119,15 @@ CASES = [
     ([23, 9], 2, 1, 8, True, 3),
     ([16], 8, 2, 64, True, 1),
     ([31], 4, 2, 8, True, 5),
+    ([40, 7], 4, 2, 128, True, 0),    # head_dim 128
+    ([12], 2, 1, 128, False, 0),
 ]
 
 
 @pytest.mark.parametrize("case", CASES)
 def test_oracle_matches_sdpa_with_virtual_sink_key(case):
     lengths, Hq, Hkv, d, causal, window = case
-    rng = np.random.default_rng(hash(str(case)) % 2**32)
+    rng = np.random.default_rng(zlib.crc32(str(case).encode()))  # stable across processes
     q, k, v, do, s, cu = rand_case(rng, lengths, Hq, Hkv, d)
     scale = 1.0 / math.sqrt(d)
     got = oracle.sinkattn(q, k, v, s, cu, causal=causal, window=window, scale=scale,
