@@ -11,9 +11,11 @@ pairs the mask allows: forward 4*d per pair and head, backward 10*d
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                     [--workload dense|window|varlen|long|long_window|tiny|decode|decode_window]
 
-For N > 1 launch under torch.distributed.run: every rank runs its own batch
-(no collective on the data path), timing is the max over ranks, and value is
-the total over ranks. --impl reference times the fp64 CPU oracle on a
+For N > 1 every rank (one process per GPU, under torch.distributed.run; a
+plain ``python bench.py --gpus N`` starts that launcher itself) runs the step
+on its own batch, data parallel: the only exchange is the all-reduce of the
+per-head sink gradient dL/dS_h after each backward (NCCL). Timing is the max
+over ranks and value the total over ranks (weak scaling). --impl reference times the fp64 CPU oracle on a
 bounded sample of the same workload (rank 0 only).
 
 The decode workloads time one decode step (a query row per sequence over a
@@ -299,7 +301,7 @@ def run_gb300(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
 
-    from attention_learnable_sinks_gb300 import _binding, api, workloads
+    from attention_learnable_sinks_gb300 import _binding, api, sharding, workloads
     _binding.lib()
     w = workloads.config(args.workload)
     lengths = w.meta["lengths"]
@@ -343,6 +345,8 @@ def run_gb300(args):
                      scale=w.scale, dq=dq, dk=dk, dv=dv, dsinks=ds, workspace=ws_b,
                      timing_events=None if i is None else bwd_ev[i], deterministic=det,
                      timing_events_dq=None if i is None or not det else dq_ev[i])
+        if world > 1:  # data parallel: sum the ranks' sink gradients
+            sharding.all_reduce_sink_grad(ds)
 
     for _ in range(args.warmup):
         step()
@@ -456,11 +460,14 @@ def run_gb300(args):
     nominal = props_n.multi_processor_count * clk.get("sm_max_mhz", 0) * 1e6 * 8192 / 1e12 \
         if clk.get("sm_max_mhz") else None
 
+    cfg = workload_config(w, args.workload)
+    cfg["parallelism"] = (f"dp{world}: each rank its own batch, dL/dS_h all-reduced per step"
+                          if world > 1 else "single GPU")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
-        "config": workload_config(w, args.workload),
+        "config": cfg,
         "frac_of_peak": value / world / peak, "peak_tflops": peak, "peak_source": peak_src,
         "peak_nominal_tflops": nominal,
         "frac_of_nominal_peak": (value / world / nominal) if nominal else None,
@@ -693,6 +700,22 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: start the launcher with this same command line
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               "--master-port", str(port), os.path.abspath(__file__),
+               *(sys.argv[1:] if argv is None else argv)]
+        return subprocess.call(cmd)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} does not match WORLD_SIZE={world} of the launcher")
     if args.workload.startswith("decode"):
         return run_decode(args)
     if args.impl == "reference":
