@@ -74,6 +74,8 @@ SYMBOLS = [
     ("sinkattn_device_error", ctypes.c_int32, [ctypes.c_int32]),
     ("sinkattn_launch_count", ctypes.c_uint64, []),
     ("sinkattn_params_size", ctypes.c_size_t, [ctypes.c_int32]),
+    ("sinkattn_set_wait_limit_ns", None, [ctypes.c_uint64]),
+    ("sinkattn_test_withhold_copies", None, [ctypes.c_int32]),
 ]
 
 STATUS = {0: "SINKATTN_OK", 1: "SINKATTN_ERR_INVALID_ARG", 2: "SINKATTN_ERR_UNSUPPORTED",

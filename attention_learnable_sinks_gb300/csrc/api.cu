@@ -16,9 +16,13 @@ namespace sinkattn {
 
 namespace {
 
+constexpr uint64_t sm100_default_wait_ns() { return 2000000000ull; }  // 2 s, as in sm100.cuh
+
 __device__ int32_t g_error_word;  // first error recorded by any kernel
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_limit_ns{sm100_default_wait_ns()};
+std::atomic<int32_t> g_withhold{0};
 thread_local std::string g_message;
 
 constexpr int kMaxDevices = 64;
@@ -163,6 +167,8 @@ sinkattn_status check_fwd(const sinkattn_fwd_params* a, Problem* p) {
   p->window = (a->window > 0 && a->window < a->max_seqlen) ? a->window : 0;
   p->scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
   p->scale_log2 = p->scale * 1.4426950408889634f;
+  p->wait_limit_ns = wait_limit_ns();
+  p->withhold_copies = withhold_copies();
   return SINKATTN_OK;
 }
 
@@ -196,6 +202,9 @@ EncodeTiledFn encode_tiled() {
 }
 
 }  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int32_t withhold_copies() { return g_withhold.load(std::memory_order_relaxed); }
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
@@ -432,6 +441,8 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
   p.split_chunks = (int32_t)per;
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_ns();
+  p.withhold_copies = withhold_copies();
   const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode kernels");
   return SINKATTN_OK;
@@ -468,6 +479,14 @@ int32_t sinkattn_device_error(int32_t reset) {
 }
 
 uint64_t sinkattn_launch_count(void) { return g_launches.load(); }
+
+void sinkattn_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns ? ns : sm100_default_wait_ns(), std::memory_order_relaxed);
+}
+
+void sinkattn_test_withhold_copies(int32_t on) {
+  g_withhold.store(on ? 1 : 0, std::memory_order_relaxed);
+}
 
 size_t sinkattn_params_size(int32_t which) {
   if (which == 0) return sizeof(sinkattn_fwd_params);

@@ -210,7 +210,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
   const Problem& p = bp.f;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const Guard g{&sm.abort, p.err};
+  const Guard g{&sm.abort, p.err, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
@@ -278,6 +278,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         ++nsched;
       }
       if (w < 0) break;
+      if (p.withhold_copies) break;  // test hook: the consumers' waits run out
       const Unit u = decode(p, items, w);
       // the unit's K / V load goes out right after its first Q / dO tile: a
       // Q / dO stage frees up a few tiles before the previous unit's K / V

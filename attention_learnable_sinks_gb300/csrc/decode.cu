@@ -134,7 +134,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
     }
     return;
   }
-  const Guard g{&sm.abort, p.err};
+  const Guard g{&sm.abort, p.err, p.wait_limit_ns};
   if (t == 0) {
     sm.abort = 0;
     sm.bad = len_ok ? 0 : 1;
@@ -245,7 +245,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
   int n_tma = 0;  // chunks whose copies were issued (warp 0)
   int n_s = 0;    // chunks whose S^T was issued (warp 0)
   if (warp == 0) {
-    for (; n_tma < kStages && n_tma < nlocal; ++n_tma)
+    // (test hook: with copies withheld, every wait below runs out)
+    for (; n_tma < kStages && n_tma < nlocal && !p.withhold_copies; ++n_tma)
       issue_tma(n_tma, lane < nbox ? sm.blk[n_tma * nbox + lane] : 0);
     if (mbar_wait_warp(&sm.full[0], 0, g)) {
       tc_fence_after();

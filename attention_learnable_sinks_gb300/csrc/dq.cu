@@ -100,7 +100,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
   const Problem& p = bp.f;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const Guard g{&sm.abort, p.err};
+  const Guard g{&sm.abort, p.err, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
@@ -158,6 +158,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         mbar_arrive(&sm.sched_full[s]);
         ++nsched;
         if (w < 0) break;
+        if (p.withhold_copies) break;  // test hook: the consumers' waits run out
         const int qb = nq & 1;
         if (!mbar_wait(&sm.q_empty[qb], ((nq >> 1) & 1) ^ 1, g)) break;
         mbar_expect_tx(&sm.q_full[qb], 2 * kTileBytes);

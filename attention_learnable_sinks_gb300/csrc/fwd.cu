@@ -120,7 +120,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const Guard g{&sm.abort, p.err};
+  const Guard g{&sm.abort, p.err, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
@@ -199,6 +199,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_arrive(&sm.sched_full[s]);
         ++nsched;
         if (w < 0) break;
+        if (p.withhold_copies) break;  // test hook: the consumers' waits run out
         if (!mbar_wait(&sm.q_empty, (nq & 1) ^ 1, g)) break;
         mbar_expect_tx(&sm.q_full, kTileBytes);
         tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base + u.r0);

@@ -27,6 +27,9 @@ struct Problem {
   float scale;                 // softmax scale
   float scale_log2;            // scale * log2(e)
   int32_t* err;                // device error word
+  uint64_t wait_limit_ns;      // time limit of every wait inside the kernels
+  int32_t withhold_copies;     // test hook: producers issue no copies (the
+                               // consumers' waits run out)
 };
 
 struct BwdProblem {
@@ -64,6 +67,8 @@ struct DecodeProblem {
   int32_t split_chunks;          // 128-key chunks per split
   float scale_log2;              // softmax scale * log2(e)
   int32_t* err;                  // device error word
+  uint64_t wait_limit_ns;        // time limit of every wait inside the kernels
+  int32_t withhold_copies;       // test hook: the split kernel issues no copies
 };
 
 // Tile work list in the workspace: meta[0] = number of items, meta[1] = the
@@ -134,6 +139,11 @@ cudaError_t launch_bwd_dq(const BwdProblem& p, const BwdLaunch& l, const TileLis
 
 size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit);
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t s);
+
+// The limit of the waits inside kernels and the copy-withholding test hook,
+// as set by sinkattn_set_wait_limit_ns / sinkattn_test_withhold_copies.
+uint64_t wait_limit_ns();
+int32_t withhold_copies();
 
 // Counts kernel launches (sinkattn_launch_count).
 void note_launch(int n = 1);

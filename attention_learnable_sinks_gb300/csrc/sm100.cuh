@@ -2,11 +2,12 @@
 // waits, TMA tensor loads, tensor-memory (TMEM) allocation / loads / stores,
 // and tcgen05 (UMMA) descriptors and issue.
 //
-// Every wait here is bounded. A wait that does not complete within
-// kWaitLimitNs of global time sets the CTA's abort flag and the library's
-// device error word (SINKATTN_ERR_TIMEOUT) and returns false; once the abort
-// flag is set, every other wait returns false at once, so a stuck pipeline
-// drains in bounded time instead of hanging the GPU.
+// Every wait here is bounded. A wait that does not complete within the
+// call's limit (Guard::limit, 2 s unless the caller set another) of global
+// time sets the CTA's abort flag and the library's device error word
+// (SINKATTN_ERR_TIMEOUT) and returns false; once the abort flag is set, every
+// other wait returns false at once, so a stuck pipeline drains in bounded time
+// instead of hanging the GPU.
 #pragma once
 
 #include <cuda.h>
@@ -15,6 +16,8 @@
 namespace sinkattn {
 namespace sm100 {
 
+// Default limit of a wait, and the limit of the drain waits a CTA makes for
+// its own copies and products before it exits after an abort.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kErrTimeout = 5;                    // SINKATTN_ERR_TIMEOUT
 
@@ -73,6 +76,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 struct Guard {
   volatile int* abort;  // in shared memory
   int32_t* err;         // device error word (global)
+  uint64_t limit;       // time limit of a wait, ns
   __device__ __forceinline__ bool aborted() const { return *abort != 0; }
   __device__ __forceinline__ void fail(int code) const {
     *abort = 1;
@@ -92,7 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (g.aborted()) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > g.limit) {
       g.fail(kErrTimeout);
       return false;
     }

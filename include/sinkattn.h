@@ -238,6 +238,26 @@ SINKATTN_API const char* sinkattn_last_error_message(void);
  * Returns SINKATTN_ERR_CUDA if the word cannot be read. */
 SINKATTN_API int32_t sinkattn_device_error(int32_t reset);
 
+/* Time limit, in nanoseconds, of every wait inside the library's kernels
+ * (an mbarrier phase, a copy landing, a product completing). 0 restores the
+ * default of 2 s. It applies to calls enqueued after it, from any thread. A
+ * wait that runs out records SINKATTN_ERR_TIMEOUT in the device error word;
+ * the kernel then stops its other waits, lets the copies and products it
+ * issued finish, frees its tensor memory and returns, so the CUDA context stays
+ * usable. No passage of the pages corresponds to this: it is the library's
+ * watchdog. */
+SINKATTN_API void sinkattn_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for that watchdog. While on (nonzero), the copy-issuing warp of
+ * every pipelined kernel -- the forward, the backward main kernel, the
+ * deterministic dq pass and the decode split kernel -- hands out its first
+ * work item and then issues no copies, so the warps waiting for them run into
+ * the wait limit: the call records SINKATTN_ERR_TIMEOUT, its outputs are
+ * undefined, and nothing faults. Applies to calls enqueued after it. Off by
+ * default; a test turns it on with a short wait limit and off again. No
+ * passage of the pages corresponds to this. */
+SINKATTN_API void sinkattn_test_withhold_copies(int32_t on);
+
 /* Number of kernels this library has launched in this process. */
 SINKATTN_API uint64_t sinkattn_launch_count(void);
 

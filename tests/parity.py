@@ -26,10 +26,45 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+# Guard regions around every output and workspace the library writes. A
+# store outside its tensor (a ragged tail tile, a wrong stride) lands in a
+# guard and changes it; the bodies start as the same pattern, so an element
+# the library never writes stays NaN and fails the comparison.
+GUARD_BYTES = 4096
+_CANARY = {torch.bfloat16: (torch.int16, 0x7FA5),     # a bf16 NaN no kernel produces
+           torch.float32: (torch.int32, 0x7FC0A5A5),  # an fp32 NaN payload
+           torch.uint8: (torch.uint8, 0xA5)}
+
+
+class Guarded:
+    """A device tensor of ``shape`` inside a larger buffer whose head and tail
+    (GUARD_BYTES each) hold a canary bit pattern, as does the body at first."""
+
+    def __init__(self, shape, dtype, device):
+        ity, pat = _CANARY[dtype]
+        esz = torch.empty(0, dtype=dtype).element_size()
+        self.n = int(np.prod(shape)) if len(shape) else 1
+        self.pad = GUARD_BYTES // esz
+        self.buf = torch.empty(self.n + 2 * self.pad, dtype=dtype, device=device)
+        self.bits = self.buf.view(ity)
+        self.bits.fill_(pat)
+        self.pattern = pat
+        self.t = self.buf[self.pad:self.pad + self.n].view(shape)
+
+    def check(self, name):
+        head = self.bits[:self.pad]
+        tail = self.bits[self.pad + self.n:]
+        pat = self.pattern
+        assert bool((head == pat).all()), f"{name}: guard region before the tensor was overwritten"
+        assert bool((tail == pat).all()), f"{name}: guard region after the tensor was overwritten"
+
+
 def run_cuda(w: Workload, device="cuda", q_view=None, k_view=None, v_view=None, scale=None,
              sinks=True, deterministic=False):
     """One forward + backward through the C ABI; returns fp64 host arrays.
-    ``deterministic`` selects the backward whose dq is summed in a fixed order."""
+    ``deterministic`` selects the backward whose dq is summed in a fixed order.
+    Every output and both workspaces sit between guard regions that must come
+    back unchanged."""
     q = q_view if q_view is not None else w.q.to(device)
     k = k_view if k_view is not None else w.k.to(device)
     v = v_view if v_view is not None else w.v.to(device)
@@ -37,14 +72,30 @@ def run_cuda(w: Workload, device="cuda", q_view=None, k_view=None, v_view=None, 
     cu = w.cu_seqlens.to(device)
     do = w.dout.to(device)
     sc = w.scale if scale is None else scale
+    total, Hq, Hkv, d = w.total, w.Hq, w.Hkv, 64
+    nseq = w.nseq
+    bf, f32 = torch.bfloat16, torch.float32
+    g = {"o": Guarded((total, Hq, d), bf, device), "lse": Guarded((Hq, total), f32, device),
+         "dq": Guarded((total, Hq, d), bf, device), "dk": Guarded((total, Hkv, d), bf, device),
+         "dv": Guarded((total, Hkv, d), bf, device), "dsinks": Guarded((Hq,), f32, device),
+         "ws_fwd": Guarded((max(api.workspace_bytes("fwd", nseq, total, Hq, Hkv), 1),),
+                           torch.uint8, device),
+         "ws_bwd": Guarded((max(api.workspace_bytes("bwd", nseq, total, Hq, Hkv), 1),),
+                           torch.uint8, device)}
     o, lse = api.forward(q, k, v, s, cu, max(w.max_seqlen, 1), causal=w.causal, window=w.window,
-                         scale=sc)
+                         scale=sc, out=g["o"].t, lse=g["lse"].t, workspace=g["ws_fwd"].t)
     dq, dk, dv, ds = api.backward(q, k, v, s, cu, max(w.max_seqlen, 1), o, lse, do,
                                   causal=w.causal, window=w.window, scale=sc,
-                                  deterministic=deterministic)
+                                  dq=g["dq"].t, dk=g["dk"].t, dv=g["dv"].t,
+                                  dsinks=g["dsinks"].t if sinks else None,
+                                  workspace=g["ws_bwd"].t, deterministic=deterministic)
     torch.cuda.synchronize()
     err = _binding.device_error(reset=True)
     assert err == 0, f"device error word {err}"
+    for name, gt in g.items():
+        if name == "dsinks" and not sinks:
+            continue
+        gt.check(name)
     out = {"o": f64(o), "lse": f64(lse), "dq": f64(dq), "dk": f64(dk), "dv": f64(dv)}
     out["dsinks"] = f64(ds) if ds is not None else np.zeros(w.Hq)
     return out

@@ -54,7 +54,8 @@ def compare(w, got, ref, seqs=None):
                 rel = np.linalg.norm(o[b, h] - ro[b, h]) / n
                 assert rel <= TOL_REL, f"o seq {b} head {h}: rel L2 {rel:.3g}"
         same = lse[:, b] == rlse[:, b]  # equal infinities included
-        err = np.where(same, 0.0, np.abs(np.where(same, 0.0, lse[:, b] - rlse[:, b])))
+        diff = np.subtract(lse[:, b], rlse[:, b], out=np.zeros_like(rlse[:, b]), where=~same)
+        err = np.abs(diff)
         assert np.all(err <= TOL_LSE), f"lse seq {b}: max err {err.max():.3g}"
 
 
