@@ -64,6 +64,7 @@ class DecodeParams(ctypes.Structure):
 SYMBOLS = [
     ("sinkattn_fwd_workspace_size", ctypes.c_size_t, [ctypes.c_int32] * 5),
     ("sinkattn_bwd_workspace_size", ctypes.c_size_t, [ctypes.c_int32] * 5),
+    ("sinkattn_bwd_workspace_size_mode", ctypes.c_size_t, [ctypes.c_int32] * 6),
     ("sinkattn_fwd", ctypes.c_int, [ctypes.POINTER(FwdParams), _c_void_p]),
     ("sinkattn_bwd", ctypes.c_int, [ctypes.POINTER(BwdParams), _c_void_p]),
     ("sinkattn_bwd_static_workspace", ctypes.c_int, [ctypes.POINTER(BwdParams), _c_void_p]),

@@ -177,10 +177,15 @@ def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, s
     return o, lse
 
 
-def workspace_bytes(kind: str, nseq: int, total: int, Hq: int, Hkv: int) -> int:
+def workspace_bytes(kind: str, nseq: int, total: int, Hq: int, Hkv: int,
+                    deterministic: bool = False) -> int:
+    """Workspace bytes of the forward ("fwd") or of the backward ("bwd") in the
+    given mode (the deterministic backward needs no fp32 dq accumulator)."""
     L = _binding.lib()
-    fn = L.sinkattn_fwd_workspace_size if kind == "fwd" else L.sinkattn_bwd_workspace_size
-    return int(fn(nseq, total, Hq, Hkv, HEAD_DIM))
+    if kind == "fwd":
+        return int(L.sinkattn_fwd_workspace_size(nseq, total, Hq, Hkv, HEAD_DIM))
+    return int(L.sinkattn_bwd_workspace_size_mode(nseq, total, Hq, Hkv, HEAD_DIM,
+                                                  1 if deterministic else 0))
 
 
 class _SinkAttention(torch.autograd.Function):

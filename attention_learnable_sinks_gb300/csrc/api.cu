@@ -75,14 +75,23 @@ sinkattn_status device_info(int32_t** err, int* sms) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The backward hands out key tiles sequence by sequence above this fp32 dq
+// accumulator size (1.5x the 126 MB L2). Measured on GB300: the 2.2 GB
+// accumulator of the 32-sequence varlen batch, 24.6 -> 17.5 ms for the main
+// kernel; the 128 MB one of four 2048-token sequences, 5% slower, so it keeps
+// the order by cost.
+constexpr size_t kSeqMajorAccBytes = size_t(192) << 20;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Workspace layout. Forward: [meta | q-tile items]. Backward:
-// [meta | k-tile items | D | sink partials | dq_acc | meta | q-tile items]
-// (the query-tile list serves the deterministic dq pass).
+// [meta | k-tile items | D | sink partials | meta | q-tile items | dq_acc]
+// (the query-tile list serves the deterministic dq pass, which has no use for
+// the fp32 dq accumulator: that mode needs only the bytes before it).
 struct Layout {
   size_t q_meta, q_items, k_meta, k_items, D, part, dq_acc, bytes;
   int32_t capacity, nchunks;
+  size_t bytes_for(bool deterministic) const { return deterministic ? dq_acc : bytes; }
 };
 
 Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
@@ -104,12 +113,12 @@ Layout layout(int32_t nseq, int32_t total, int32_t Hq, bool bwd) {
     off += align256(sizeof(float) * (size_t)Hq * total);
     l.part = off;
     off += align256(sizeof(float) * 8 * (size_t)Hq * l.capacity);
-    l.dq_acc = off;
-    off += align256(sizeof(float) * (size_t)total * Hq * kHeadDim);
     l.q_meta = off;
     off += 256;
     l.q_items = off;
     off += align256(sizeof(int2) * (size_t)l.capacity);
+    l.dq_acc = off;
+    off += align256(sizeof(float) * (size_t)total * Hq * kHeadDim);
   }
   l.bytes = off;
   return l;
@@ -218,9 +227,12 @@ cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, i
   const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)row_stride * 2};
   const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)box_rows};
   const cuuint32_t elem[3] = {1, 1, 1};
+  // a box row is 128 bytes, one head of one token; promoting the L2 fill to
+  // 256 bytes would also fetch the neighbouring head's row (measured 12%
+  // slower on the 32-sequence varlen backward, no faster elsewhere)
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -252,8 +264,13 @@ size_t sinkattn_fwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int3
 
 size_t sinkattn_bwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
                                    int32_t head_dim) {
+  return sinkattn_bwd_workspace_size_mode(nseq, total, Hq, Hkv, head_dim, 0);
+}
+
+size_t sinkattn_bwd_workspace_size_mode(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
+                                        int32_t head_dim, int32_t deterministic) {
   if (!shape_ok(nseq, total, Hq, Hkv) || head_dim != kHeadDim) return 0;
-  return layout(nseq, total, Hq, true).bytes;
+  return layout(nseq, total, Hq, true).bytes_for(deterministic != 0);
 }
 
 sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
@@ -275,7 +292,7 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
   FwdLaunch fl;
   cudaError_t e = prepare_fwd(p, &fl);
   if (e != cudaSuccess) return cuda_fail(e, "forward tensor maps");
-  e = launch_build_tile_list(p, 0, qt, s);
+  e = launch_build_tile_list(p, 0, 0, qt, s);
   if (e != cudaSuccess) return cuda_fail(e, "tile list");
   record(a->timing_events[0], s);
   e = launch_fwd(p, fl, qt, sms, s);
@@ -298,8 +315,9 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
       return fail(SINKATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   }
   const Layout l = layout(f.nseq, f.total, f.Hq, true);
-  if (!a->workspace || a->workspace_bytes < l.bytes)
-    return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_bwd_workspace_size()");
+  if (!a->workspace || a->workspace_bytes < l.bytes_for(a->deterministic != 0))
+    return fail(SINKATTN_ERR_WORKSPACE,
+                "workspace missing or smaller than sinkattn_bwd_workspace_size_mode()");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (f.total == 0) {
     if (a->dsinks && !a->accumulate_dsinks) {
@@ -332,10 +350,14 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   cudaError_t e = prepare_bwd_main(bp, &bl);
   if (e == cudaSuccess && bp.deterministic) e = prepare_bwd_dq();
   if (e != cudaSuccess) return cuda_fail(e, "backward tensor maps");
-  e = launch_build_tile_list(bp.f, 1, kt, s);
+  // Key tiles sequence by sequence when the fp32 dq accumulator is well
+  // beyond L2 (the running units then share their sequences' rows of it).
+  const bool seq_major = !bp.deterministic && bp.f.nseq > 1 &&
+                         (size_t)bp.f.total * bp.f.Hq * kHeadDim * sizeof(float) > kSeqMajorAccBytes;
+  e = launch_build_tile_list(bp.f, 1, seq_major ? 1 : 0, kt, s);
   if (e != cudaSuccess) return cuda_fail(e, "key-tile list");
   if (bp.deterministic) {
-    e = launch_build_tile_list(bp.f, 0, qt, s);
+    e = launch_build_tile_list(bp.f, 0, 0, qt, s);
     if (e != cudaSuccess) return cuda_fail(e, "query-tile list");
   }
   e = launch_bwd_preprocess(bp, s);

@@ -111,8 +111,10 @@ cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, i
 cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int total);
 
 // Launchers (each returns the cudaGetLastError() of its launch).
-cudaError_t launch_build_tile_list(const Problem& p, int by_keys, const TileList& list,
-                                   cudaStream_t s);
+// seq_major: sequence by sequence, each by decreasing cost (else by decreasing
+// cost over the whole batch).
+cudaError_t launch_build_tile_list(const Problem& p, int by_keys, int seq_major,
+                                   const TileList& list, cudaStream_t s);
 // Tensor maps and kernel attributes are prepared before a call's first
 // launch, so that its kernels go out back to back (host-side preparation
 // between two launches would leave the GPU idle).

@@ -1,12 +1,24 @@
 // Varlen tile scheduler: builds, on the device, the list of 128-row query
-// tiles (forward) or 128-key key tiles (backward) of a packed batch, ordered by
-// decreasing cost so that persistent CTAs taking items in order approximate a
-// longest-processing-time-first schedule. Building on the device keeps the
-// whole call asynchronous (no host copy of cu_seqlens, no stream sync).
+// tiles (forward) or 128-key key tiles (backward) of a packed batch, so that
+// persistent CTAs taking items in order approximate a longest-processing-time-
+// first schedule. Building on the device keeps the whole call asynchronous (no
+// host copy of cu_seqlens, no stream sync).
 //
 // Cost of a query tile = number of key tiles it sees; cost of a key tile =
 // number of query tiles that see it. Both follow from the causal / window
 // mask and the sequence length.
+//
+// Two orders:
+//   by cost           decreasing cost over the whole batch (the default)
+//   sequence-major    sequence 0's tiles, then sequence 1's, ..., each
+//                     sequence's by decreasing cost. Used for the backward
+//                     when its fp32 dq accumulator is far larger than L2: the
+//                     running units then cover one or two sequences, whose
+//                     accumulator rows and Q / dO tiles stay in L2, instead of
+//                     every sequence at once (on the 32-sequence varlen batch
+//                     the backward main kernel took 17.5 ms instead of 24.6).
+//                     When the batch has more sequences than the bucket table
+//                     separates, the later ones share the last bucket.
 #include "internal.h"
 
 namespace sinkattn {
@@ -27,11 +39,20 @@ __device__ inline int tile_cost(int by_keys, int causal, int window, int L, int 
   return (hi + kTile - 1) / kTile - lo / kTile;
 }
 
+// Bucket of a tile: buckets are handed out from the highest index down.
+__device__ inline int bucket_of(int seq_major, int levels, int b, int cost) {
+  if (!seq_major) return min(cost, kBuckets - 1);
+  const int key = b * levels + (levels - 1 - min(cost, levels - 1));
+  return kBuckets - 1 - min(key, kBuckets - 1);
+}
+
 __global__ void __launch_bounds__(kThreads)
 build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int max_seqlen,
-                       int causal, int window, int by_keys, int capacity,
+                       int causal, int window, int by_keys, int seq_major, int capacity,
                        int2* __restrict__ items, int32_t* __restrict__ meta,
                        int32_t* __restrict__ err) {
+  // cost levels per sequence in sequence-major order
+  const int levels = seq_major ? max(1, kBuckets / max(nseq, 1)) : 1;
   __shared__ int hist[kBuckets];
   __shared__ int warp_sums[kThreads / 32];
   __shared__ int bad;
@@ -51,7 +72,7 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
     }
     const int nt = (L + kTile - 1) / kTile;
     for (int t = lane; t < nt; t += 32)
-      atomicAdd(&hist[min(tile_cost(by_keys, causal, window, L, t), kBuckets - 1)], 1);
+      atomicAdd(&hist[bucket_of(seq_major, levels, b, tile_cost(by_keys, causal, window, L, t))], 1);
   }
   __syncthreads();
   if (bad) {
@@ -63,7 +84,7 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
     return;
   }
 
-  // exclusive scan in order of decreasing cost: thread t owns the four
+  // exclusive scan in order of decreasing bucket: thread t owns the four
   // buckets kBuckets-1-4t ... kBuckets-4-4t
   constexpr int kPer = kBuckets / kThreads;
   int local[kPer];
@@ -115,7 +136,7 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
     const int L = cu[b + 1] - cu[b];
     const int nt = (L + kTile - 1) / kTile;
     for (int t = lane; t < nt; t += 32) {
-      const int c = min(tile_cost(by_keys, causal, window, L, t), kBuckets - 1);
+      const int c = bucket_of(seq_major, levels, b, tile_cost(by_keys, causal, window, L, t));
       const int pos = atomicAdd(&hist[c], 1);
       items[pos] = make_int2(b, t);
     }
@@ -128,11 +149,11 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
 
 }  // namespace
 
-cudaError_t launch_build_tile_list(const Problem& p, int by_keys, const TileList& list,
-                                   cudaStream_t s) {
+cudaError_t launch_build_tile_list(const Problem& p, int by_keys, int seq_major,
+                                   const TileList& list, cudaStream_t s) {
   build_tile_list_kernel<<<1, kThreads, 0, s>>>(p.cu, p.nseq, p.total, p.max_seqlen, p.causal,
-                                                p.window, by_keys, list.capacity, list.items,
-                                                list.meta, p.err);
+                                                p.window, by_keys, seq_major, list.capacity,
+                                                list.items, list.meta, p.err);
   note_launch();
   return cudaGetLastError();
 }

@@ -36,7 +36,8 @@ extern "C" SINKATTN_API sinkattn_status sinkattn_bwd_static_workspace(
     const sinkattn_bwd_params* params, void* stream) {
   if (!params) return sinkattn_bwd(nullptr, stream);  // reports the NULL argument
   const sinkattn_fwd_params& f = params->fwd;
-  const size_t need = sinkattn_bwd_workspace_size(f.nseq, f.total, f.Hq, f.Hkv, f.head_dim);
+  const size_t need =
+      sinkattn_bwd_workspace_size_mode(f.nseq, f.total, f.Hq, f.Hkv, f.head_dim, params->deterministic);
   if (need > SINKATTN_STATIC_BWD_WORKSPACE_BYTES) {
     sinkattn::note_error_message(
         "problem needs " + std::to_string(need) + " bytes of workspace; the static workspace holds " +
@@ -46,9 +47,15 @@ extern "C" SINKATTN_API sinkattn_status sinkattn_bwd_static_workspace(
   }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (e != cudaSuccess) {
     sinkattn::note_error_message(std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     return SINKATTN_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    sinkattn::note_error_message("current device " + std::to_string(dev) +
+                                 " is beyond the " + std::to_string(kMaxDevices) +
+                                 " devices the static workspace keeps addresses for");
+    return SINKATTN_ERR_UNSUPPORTED;
   }
   void* ws = nullptr;
   {

@@ -139,11 +139,17 @@ typedef struct sinkattn_bwd_params {
                                   (ignored when deterministic = 0)           */
 } sinkattn_bwd_params;
 
-/* Workspace sizes in bytes for a problem of this shape (0 on bad input). */
+/* Workspace sizes in bytes for a problem of this shape (0 on bad input).
+ * sinkattn_bwd_workspace_size covers either backward mode; the deterministic
+ * one needs no fp32 dq accumulator, and sinkattn_bwd_workspace_size_mode gives
+ * the size for the chosen mode (deterministic != 0: the smaller one). */
 SINKATTN_API size_t sinkattn_fwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
                                    int32_t head_dim);
 SINKATTN_API size_t sinkattn_bwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
                                    int32_t head_dim);
+SINKATTN_API size_t sinkattn_bwd_workspace_size_mode(int32_t nseq, int32_t total, int32_t Hq,
+                                                     int32_t Hkv, int32_t head_dim,
+                                                     int32_t deterministic);
 
 /* Enqueue the forward / backward on `stream`. */
 SINKATTN_API sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* params, void* stream);
@@ -159,9 +165,12 @@ SINKATTN_API sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* params, voi
  *
  * The scratch memory is one array inside the library of
  * SINKATTN_STATIC_BWD_WORKSPACE_BYTES bytes, held by every GPU that loads the
- * library until the process exits. A problem whose
- * sinkattn_bwd_workspace_size() exceeds it returns SINKATTN_ERR_WORKSPACE and
- * launches nothing. The array's device address is looked up on the first call
+ * library until the process exits. A problem whose workspace for the chosen
+ * mode, sinkattn_bwd_workspace_size_mode(..., params->deterministic), exceeds
+ * it returns SINKATTN_ERR_WORKSPACE and launches nothing. The atomic mode needs
+ * 256 bytes of fp32 dq accumulator per (token, query head), so it fits up to
+ * about 250 000 (token, query head) rows; the deterministic mode needs a few
+ * bytes per row and fits far larger problems. The array's device address is looked up on the first call
  * made on each device (with that device current), so make that first call
  * before any stream capture. Every call shares the array and it keeps the
  * last call's contents (nothing in it needs to start at zero); calls that
