@@ -70,6 +70,7 @@ SYMBOLS = [
     ("sinkattn_bwd_static_workspace", ctypes.c_int, [ctypes.POINTER(BwdParams), _c_void_p]),
     ("sinkattn_decode_workspace_size", ctypes.c_size_t, [ctypes.c_int32] * 3),
     ("sinkattn_decode", ctypes.c_int, [ctypes.POINTER(DecodeParams), _c_void_p]),
+    ("sinkattn_decode_exact", ctypes.c_int, [ctypes.POINTER(DecodeParams), _c_void_p]),
     ("sinkattn_status_string", ctypes.c_char_p, [ctypes.c_int32]),
     ("sinkattn_last_error_message", ctypes.c_char_p, []),
     ("sinkattn_device_error", ctypes.c_int32, [ctypes.c_int32]),

@@ -133,13 +133,15 @@ def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=Tru
 
 
 def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, scale=None,
-           num_splits=0, out=None, lse=None, workspace=None):
+           num_splits=0, out=None, lse=None, workspace=None, exact=False):
     """One query row per sequence against a paged KV cache.
 
     q [nseq, Hq, 64] bf16; k_cache, v_cache [num_blocks, block_size, Hkv, 64]
     bf16; block_table [nseq, max_blocks] int32; seqlens [nseq] int32 (keys per
     sequence, the new token's included). Returns o [nseq, Hq, 64] bf16 and
-    lse [Hq, nseq] fp32: the last row of ``forward`` over each sequence."""
+    lse [Hq, nseq] fp32: the last row of ``forward`` over each sequence. With
+    ``exact`` each row is computed exactly as ``forward`` computes that last
+    row, so the two agree bit for bit (num_splits is then ignored)."""
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
@@ -160,7 +162,8 @@ def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, s
     o = out if out is not None else torch.empty(nseq, Hq, d, dtype=torch.bfloat16, device=q.device)
     lse = lse if lse is not None else torch.empty(Hq, nseq, dtype=torch.float32, device=q.device)
     if workspace is None:
-        nbytes = L.sinkattn_decode_workspace_size(nseq, Hq, num_splits if num_splits > 0 else 64)
+        nbytes = 256 if exact else L.sinkattn_decode_workspace_size(
+            nseq, Hq, num_splits if num_splits > 0 else 64)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     p = DecodeParams()
     p.q, p.k_cache, p.v_cache = _ptr(q), _ptr(k_cache), _ptr(v_cache)
@@ -173,7 +176,10 @@ def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, s
     p.window = int(window)
     p.num_splits = int(num_splits)
     p.softmax_scale = float(scale) if scale is not None else 0.0
-    check(L.sinkattn_decode(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_decode")
+    if exact:
+        check(L.sinkattn_decode_exact(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_decode_exact")
+    else:
+        check(L.sinkattn_decode(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_decode")
     return o, lse
 
 

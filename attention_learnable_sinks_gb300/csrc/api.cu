@@ -237,6 +237,21 @@ cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, i
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_bf16_heads(CUtensorMap* map, const void* base, int heads, int rows,
+                                 int box_heads) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)box_heads, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                         strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int total) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
@@ -382,8 +397,14 @@ size_t sinkattn_decode_workspace_size(int32_t nseq, int32_t Hq, int32_t num_spli
   return decode_workspace_bytes(nseq, Hq, num_splits);
 }
 
-sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
-  g_message.clear();
+}  // extern "C"
+
+namespace {
+
+// Checks shared by both decode entry points (nothing to do: nseq == 0 gives
+// SINKATTN_OK with *empty set).
+sinkattn_status check_decode(const sinkattn_decode_params* a, bool* empty) {
+  *empty = false;
   if (!a) return fail(SINKATTN_ERR_INVALID_ARG, "params is NULL");
   if (a->head_dim != kHeadDim) return fail(SINKATTN_ERR_UNSUPPORTED, "head_dim must be 64");
   if (a->nseq < 0 || a->nseq > 65535 || a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv || a->Hq > 65535)
@@ -401,11 +422,26 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
     return fail(SINKATTN_ERR_INVALID_ARG, "num_splits must be in [0, 64]");
   if (std::isnan(a->softmax_scale) || std::isinf(a->softmax_scale))
     return fail(SINKATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
-  if (a->nseq == 0) return SINKATTN_OK;
+  if (a->nseq == 0) {
+    *empty = true;
+    return SINKATTN_OK;
+  }
   if (!a->q || !a->k_cache || !a->v_cache || !a->block_table || !a->seqlens || !a->o)
     return fail(SINKATTN_ERR_INVALID_ARG, "q, k_cache, v_cache, block_table, seqlens and o must be non-NULL");
   if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->o))
     return fail(SINKATTN_ERR_INVALID_ARG, "q, the caches and o must be 16-byte aligned");
+  return SINKATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
+  g_message.clear();
+  bool empty = false;
+  sinkattn_status st0 = check_decode(a, &empty);
+  if (st0 != SINKATTN_OK || empty) return st0;
   if (!a->workspace ||
       a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, std::max(a->num_splits, 1)))
     return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_decode_workspace_size()");
@@ -467,6 +503,40 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
   p.withhold_copies = withhold_copies();
   const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode kernels");
+  return SINKATTN_OK;
+}
+
+sinkattn_status sinkattn_decode_exact(const sinkattn_decode_params* a, void* stream) {
+  g_message.clear();
+  bool empty = false;
+  sinkattn_status st = check_decode(a, &empty);
+  if (st != SINKATTN_OK || empty) return st;
+  if (!a->workspace || a->workspace_bytes < 256)
+    return fail(SINKATTN_ERR_WORKSPACE, "the exact decode needs a workspace of at least 256 bytes");
+  Problem p{};
+  int sms = 0;
+  st = device_info(&p.err, &sms);
+  if (st != SINKATTN_OK) return st;
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.sinks = a->sinks;
+  p.o = static_cast<__nv_bfloat16*>(a->o);
+  p.lse = a->lse;
+  p.nseq = a->nseq;
+  p.total = a->nseq;  // lse is [Hq, nseq]
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.G = a->Hq / a->Hkv;
+  p.causal = 1;
+  p.window = a->window > 0 ? a->window : 0;
+  p.scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_ns();
+  p.withhold_copies = withhold_copies();
+  PagedKV kv{a->block_table, a->seqlens, a->num_blocks, a->block_size, a->max_blocks_per_seq};
+  const cudaError_t e = launch_decode_exact(p, kv, a->k_cache, a->v_cache,
+                                            static_cast<int32_t*>(a->workspace), sms,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "exact decode");
   return SINKATTN_OK;
 }
 

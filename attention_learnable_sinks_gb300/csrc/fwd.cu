@@ -24,6 +24,22 @@
 //               bf16 into tensor memory; final O / l and LSE
 // Tensor memory (256 columns): S [0,128) fp32, P [128,192) bf16 pairs,
 // O [192,256) fp32.
+//
+// Decode instantiation (kDecode): one new query row per sequence against a
+// paged KV cache, computed exactly as the training forward computes the last
+// row of that sequence, so o and LSE agree with it bit for bit. A work unit is
+// (sequence, kv head); its G query heads' rows sit in rows 0 .. G-1 of the
+// query tile and all stand at position L - 1. The key tiles are the training
+// forward's: 128 keys from the sequence start, in order, each loaded block by
+// block from the cache; a block past the sequence end or wholly before the
+// window is read out of bounds instead, which fills it with zeros (those keys
+// are masked; the training forward sees finite keys there, so both add
+// exact zeros), and value rows past the last key in its final block are
+// zeroed before the P V product. The softmax and the products run the very
+// same instructions as for a training row; a row's arithmetic does not depend
+// on the other rows of its tile, nor on the tile's first key tile (the
+// training forward may start one tile earlier with a fully masked tile, which
+// adds exact zeros to O, the row sum and nothing to the maximum).
 #include <algorithm>
 #include <cmath>
 
@@ -47,6 +63,9 @@ constexpr float kRescale = 8.0f;  // log2 units
 constexpr int kSchedSlots = 4;
 constexpr int kSchedConsumers = 1 + 4;  // the UMMA warp and 4 softmax warps
 
+// Training: base = the sequence's first token, r0 = the tile's first row,
+// nrows = rows in the tile, h = the query head. Decode: base = the sequence,
+// r0 = L - 1 (every row's position), nrows = G, h = the group's first head.
 struct Unit {
   int base, L, r0, nrows, h, kvh, kt0, kt1;
 };
@@ -67,6 +86,27 @@ struct __align__(1024) Smem {
   int abort;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+// Decode: sequence w / Hkv, kv head w % Hkv, its keys [0, L) and the 128-key
+// tiles the training forward's last row of the sequence would take.
+__device__ __forceinline__ Unit decode_paged(const Problem& p, const PagedKV& kv, int w) {
+  Unit u;
+  u.base = w / p.Hkv;
+  u.kvh = w % p.Hkv;
+  u.h = u.kvh * p.G;
+  u.nrows = p.G;
+  int L = kv.seqlens[u.base];
+  if (L < 0 || L > kv.max_blocks * kv.block_size) {
+    atomicCAS(p.err, 0, 1 /* SINKATTN_ERR_INVALID_ARG */);
+    L = 0;
+  }
+  u.L = L;
+  u.r0 = L - 1;
+  const int klo = p.window > 0 ? max(0, L - p.window) : 0;
+  u.kt0 = klo / kTile;
+  u.kt1 = (L + kTile - 1) / kTile;
+  return u;
+}
 
 __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int w) {
   const int2 it = items[w / p.Hq];
@@ -91,6 +131,14 @@ __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int 
 // ahead of time) and publishes it in a small ring; the UMMA warp and the
 // softmax warps read the ring in order. `lanes` = the calling lanes of the
 // warp (all of them get the same verdict).
+template <bool kDecode>
+__device__ __forceinline__ Unit decode_unit(const Problem& p, const PagedKV& kv, const int2* items, int w) {
+  if constexpr (kDecode)
+    return decode_paged(p, kv, w);
+  else
+    return decode(p, items, w);
+}
+
 template <class SmemT>
 __device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g, bool arrive,
                                          unsigned lanes, Unit& u, float& sink2) {
@@ -113,10 +161,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (global_ns() - t0 > kWaitLimitNs) break;
 }
 
+template <bool kDecode>
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_v, Problem p, const int2* __restrict__ items,
-           int32_t* __restrict__ meta) {
+           const __grid_constant__ CUtensorMap tm_v, Problem p, PagedKV kv,
+           const int2* __restrict__ items, int32_t* __restrict__ meta) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -158,17 +207,40 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   tc_fence_after();
   // broadcast so the compiler sees a warp-uniform value (UMMA operands)
   const uint32_t tmem = __shfl_sync(0xffffffffu, sm.tmem_base, 0);
-  const int nwork = meta[0] * p.Hq;
+  const int nwork = kDecode ? p.nseq * p.Hkv : meta[0] * p.Hq;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t nq = 0, nk = 0, nv = 0;
+      // a key tile: one copy, or (decode) one per cache block; a block past
+      // the sequence end or wholly before the window is read out of bounds,
+      // which fills it with zeros
+      auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, const Unit& u, int kt) {
+        if constexpr (kDecode) {
+          const int bs = kv.block_size;
+          const int klo = p.window > 0 ? max(0, u.L - p.window) : 0;
+          for (int i = 0; i < kTile / bs; ++i) {
+            const int j0 = kt * kTile + i * bs;
+            int row = kv.num_blocks * bs;  // the first row past the cache
+            if (j0 < u.L && j0 + bs > klo) {
+              const int pb = kv.block_table[(int64_t)u.base * kv.max_blocks + j0 / bs];
+              if (pb >= 0 && pb < kv.num_blocks)
+                row = pb * bs;
+              else
+                atomicCAS(p.err, 0, 1 /* SINKATTN_ERR_INVALID_ARG */);
+            }
+            tma_load_3d(dst + i * bs * 128, map, bar, 0, u.kvh, row);
+          }
+        } else {
+          tma_load_3d(dst, map, bar, 0, u.kvh, u.base + kt * kTile);
+        }
+      };
       auto load_k = [&](const Unit& u, int kt) -> bool {
         const int s = nk % kKStages;
         if (!mbar_wait(&sm.k_empty[s], ((nk / kKStages) & 1) ^ 1, g)) return false;
         mbar_expect_tx(&sm.k_full[s], kTileBytes);
-        tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, u.kvh, u.base + kt * kTile);
+        load_tile(sm.k[s], &tm_k, &sm.k_full[s], u, kt);
         ++nk;
         return true;
       };
@@ -176,7 +248,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const int s = nv % kVStages;
         if (!mbar_wait(&sm.v_empty[s], ((nv / kVStages) & 1) ^ 1, g)) return false;
         mbar_expect_tx(&sm.v_full[s], kTileBytes);
-        tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, u.kvh, u.base + kt * kTile);
+        load_tile(sm.v[s], &tm_v, &sm.v_full[s], u, kt);
         ++nv;
         return true;
       };
@@ -188,8 +260,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         Unit u{};
         float sink2 = -INFINITY;
         if (w >= 0) {
-          u = decode(p, items, w);
-          if (p.sinks) sink2 = p.sinks[u.h] * kLog2e;
+          u = decode_unit<kDecode>(p, kv, items, w);
+          if (p.sinks && !kDecode) sink2 = p.sinks[u.h] * kLog2e;
+          if (kDecode && u.kt1 <= u.kt0) {
+            // a sequence without keys: the sink alone, o = 0 and lse = S_h
+            for (int r = 0; r < u.nrows; ++r) {
+              uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)u.base * p.Hq + u.h + r) * kHeadDim);
+              for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+              if (p.lse) p.lse[(int64_t)(u.h + r) * p.total + u.base] = p.sinks ? p.sinks[u.h + r] : -INFINITY;
+            }
+            continue;
+          }
         }
         const int s = nsched % kSchedSlots;
         if (!mbar_wait(&sm.sched_empty[s], ((nsched / kSchedSlots) & 1) ^ 1, g)) break;
@@ -201,8 +282,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (w < 0) break;
         if (p.withhold_copies) break;  // test hook: the consumers' waits run out
         if (!mbar_wait(&sm.q_empty, (nq & 1) ^ 1, g)) break;
-        mbar_expect_tx(&sm.q_full, kTileBytes);
-        tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base + u.r0);
+        if (kDecode) {  // the G heads' rows of this sequence into rows 0 .. G-1
+          mbar_expect_tx(&sm.q_full, (uint32_t)u.nrows * 128u);
+          tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base);
+        } else {
+          mbar_expect_tx(&sm.q_full, kTileBytes);
+          tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base + u.r0);
+        }
         ++nq;
         // K runs one tile ahead of V (S(j+1) is issued before P V(j))
         bool ok = load_k(u, u.kt0);
@@ -276,6 +362,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           break;
         }
         ++np;
+        if constexpr (kDecode) {
+          // value rows past the sequence's last key (cache slots never
+          // written) are zeroed, as the training forward's are finite there
+          const int rs = u.L - (u.kt0 + jj) * kTile;
+          if (rs < kTile) {
+            for (int e = lane; e < (kTile - rs) * 8; e += 32)
+              *reinterpret_cast<uint4*>(sm.v[sv] + (rs + e / 8) * 128 + (e % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            fence_async_smem();
+            __syncwarp();
+          }
+        }
         tc_fence_after();
         const uint64_t bv = dV0 + sv * kStageStep;
 #pragma unroll
@@ -309,8 +406,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const volatile Unit& uv = sm.sched_u[slot];
       const int kt0 = uv.kt0;
       const int n = uv.kt1 - kt0;
-      const float sink2 = sm.sched_sink[slot];
-      const int i = uv.r0 + r;
+      // decode: every row stands at L - 1, row r is head h + r with its own sink
+      const float sink2 = kDecode ? (p.sinks && r < uv.nrows ? __ldg(p.sinks + uv.h + r) * kLog2e : -INFINITY)
+                                  : sm.sched_sink[slot];
+      const int i = kDecode ? uv.r0 : uv.r0 + r;
       const int L = uv.L;
       const int khi = p.causal ? min(i + 1, L) : L;
       const int klo = p.window > 0 ? max(0, i - p.window + 1) : 0;
@@ -418,6 +517,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int nrows = uv.nrows, row0 = uv.base + uv.r0, h = uv.h;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sched_empty[slot]);  // the slot is no longer read
+      if constexpr (kDecode) {  // row r: sequence base, head h + r
+        const int b = row0 - uv.r0;
+        if (r < nrows) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)b * p.Hq + h + r) * kHeadDim);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+          if (p.lse) p.lse[(int64_t)(h + r) * p.total + b] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
+        continue;
+      }
       // O rows through shared memory, so that each store instruction writes
       // four whole 128-byte rows instead of 16 bytes of 32 rows
       uint8_t* ost = sm.ostage[quarter];
@@ -454,7 +563,7 @@ cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l) {
   if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.k, p.Hkv, p.total, p.k_stride);
   if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.v, p.Hkv, p.total, p.v_stride);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  return cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
 }
 
 cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qtiles, int num_sms,
@@ -462,7 +571,29 @@ cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qti
   const int64_t work = (int64_t)qtiles.capacity * p.Hq;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * 2);
   if (grid <= 0) return cudaSuccess;
-  fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, p, qtiles.items, qtiles.meta);
+  fwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, p, PagedKV{}, qtiles.items,
+                                                       qtiles.meta);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_exact(const Problem& p, const PagedKV& kv, const void* k_cache,
+                                const void* v_cache, int32_t* counter, int num_sms, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  const int rows = kv.num_blocks * kv.block_size;
+  cudaError_t e = make_tmap_bf16_heads(&mq, p.q, p.Hq, p.nseq, p.G);
+  if (e == cudaSuccess)
+    e = make_tmap_bf16_rows(&mk, k_cache, p.Hkv, rows, (int64_t)p.Hkv * kHeadDim, kv.block_size);
+  if (e == cudaSuccess)
+    e = make_tmap_bf16_rows(&mv, v_cache, p.Hkv, rows, (int64_t)p.Hkv * kHeadDim, kv.block_size);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess) e = cudaMemsetAsync(counter, 0, 2 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  const int64_t work = (int64_t)p.nseq * p.Hkv;
+  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * 2);
+  if (grid <= 0) return cudaSuccess;
+  fwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p, kv, nullptr, counter);
   note_launch();
   return cudaGetLastError();
 }

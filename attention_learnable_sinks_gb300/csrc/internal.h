@@ -71,6 +71,15 @@ struct DecodeProblem {
   int32_t withhold_copies;       // test hook: the split kernel issues no copies
 };
 
+// The paged KV cache of the exact decode (the forward kernel's decode
+// instantiation): keys of sequence b, logical block i are physical block
+// block_table[b * max_blocks + i] of [num_blocks, block_size, Hkv, 64].
+struct PagedKV {
+  const int32_t* block_table;
+  const int32_t* seqlens;
+  int32_t num_blocks, block_size, max_blocks;
+};
+
 // Tile work list in the workspace: meta[0] = number of items, meta[1] = the
 // next item to hand out (work stealing), items[] = {sequence, tile} sorted by
 // decreasing cost.
@@ -106,6 +115,12 @@ __host__ __device__ inline void seeing_rows(int causal, int window, int L, int c
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
                                 int64_t row_stride, int box_rows = kTile);
 
+// TMA descriptor for a contiguous bf16 [rows, heads, 64] tensor read as boxes
+// of box_heads consecutive heads of one row: 3-D {64, heads, rows}, 128-byte
+// swizzle, box {64, box_heads, 1}.
+cudaError_t make_tmap_bf16_heads(CUtensorMap* map, const void* base, int heads, int rows,
+                                 int box_heads);
+
 // TMA descriptor for the fp32 [total, heads, 64] dq accumulator (contiguous):
 // 3-D {64, heads, total}, 128-byte swizzle, box {32, 1, 128}.
 cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int total);
@@ -128,6 +143,11 @@ cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l);
 cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l);
 cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qtiles, int num_sms,
                        cudaStream_t s);
+// Exact decode: p describes nseq query rows [nseq, Hq, 64] (q, o, lse [Hq, nseq],
+// sinks, window, scale); the keys come from kv. counter: one int of device
+// memory, zeroed here before the launch (work stealing).
+cudaError_t launch_decode_exact(const Problem& p, const PagedKV& kv, const void* k_cache,
+                                const void* v_cache, int32_t* counter, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s);
 cudaError_t launch_bwd_main(const BwdProblem& p, const BwdLaunch& l, const TileList& ktiles,
                             int num_sms, cudaStream_t s);

@@ -236,6 +236,23 @@ SINKATTN_API size_t sinkattn_decode_workspace_size(int32_t nseq, int32_t Hq, int
  * size the workspace for 64 splits then (or query it with the chosen count). */
 SINKATTN_API sinkattn_status sinkattn_decode(const sinkattn_decode_params* params, void* stream);
 
+/* Decode that agrees bit for bit with the training forward. Same parameters
+ * and layouts as sinkattn_decode (num_splits is ignored), and the same
+ * result up to rounding; here each query row is computed exactly as
+ * sinkattn_fwd computes the row at the last position of the same sequence --
+ * the same 128-key tiles from the sequence start, the same online-softmax
+ * rescaling rule and the same order of every sum -- so o and lse equal that
+ * row of sinkattn_fwd bit for bit when the cache holds the same keys and
+ * values (section "Correcting Training-Inference Mismatch via Attention
+ * Sinks": the inference engine and the training stack must give the same
+ * token probabilities). One work unit per (sequence, kv head) walks the
+ * sequence's keys in order, without splitting them, so long sequences take
+ * longer than with sinkattn_decode. workspace: at least 256 bytes (a work
+ * counter, cleared by the call). Cache slots past a sequence's last key and
+ * blocks wholly before its window are not read. Block indices out of range
+ * set SINKATTN_ERR_INVALID_ARG in the device error word and read as zeros. */
+SINKATTN_API sinkattn_status sinkattn_decode_exact(const sinkattn_decode_params* params, void* stream);
+
 /* Static description of a status code; never NULL. */
 SINKATTN_API const char* sinkattn_status_string(int32_t status);
 
