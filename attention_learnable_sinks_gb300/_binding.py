@@ -31,6 +31,7 @@ class FwdParams(ctypes.Structure):
         ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
         ("causal", ctypes.c_int32), ("window", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
+        ("bwd_workspace", _c_void_p), ("bwd_workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -44,6 +45,7 @@ class BwdParams(ctypes.Structure):
         ("accumulate_dsinks", ctypes.c_int32),
         ("deterministic", ctypes.c_int32),
         ("timing_events_dq", _c_void_p * 2),
+        ("workspace_cleared", ctypes.c_int32),
     ]
 
 

@@ -71,8 +71,11 @@ def _validate_inputs(q, k, v, sinks, cu_seqlens):
 
 
 def forward(q, k, v, sinks, cu_seqlens, max_seqlen, *, causal=True, window=0, scale=None,
-            out=None, lse=None, workspace=None, timing_events=None):
-    """O [total, Hq, 64] bf16 and LSE [Hq, total] fp32 (natural log)."""
+            out=None, lse=None, workspace=None, timing_events=None, bwd_workspace=None):
+    """O [total, Hq, 64] bf16 and LSE [Hq, total] fp32 (natural log). With
+    ``bwd_workspace`` (the workspace the backward of this same problem will
+    use) the forward also clears the backward's dq accumulator in it; pass
+    ``workspace_cleared=True`` to that backward."""
     _validate_inputs(q, k, v, sinks, cu_seqlens)
     L = _binding.lib()
     total, Hq, d = q.shape
@@ -86,6 +89,8 @@ def forward(q, k, v, sinks, cu_seqlens, max_seqlen, *, causal=True, window=0, sc
     _fill_fwd(p, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale, o, lse)
     p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
     p.timing_events[0], p.timing_events[1] = _events(timing_events)
+    if bwd_workspace is not None:
+        p.bwd_workspace, p.bwd_workspace_bytes = _ptr(bwd_workspace), bwd_workspace.numel()
     check(L.sinkattn_fwd(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_fwd")
     return o, lse
 
@@ -93,13 +98,16 @@ def forward(q, k, v, sinks, cu_seqlens, max_seqlen, *, causal=True, window=0, sc
 def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=True, window=0,
              scale=None, dq=None, dk=None, dv=None, dsinks=None, workspace=None,
              timing_events=None, accumulate_dsinks=False, deterministic=False,
-             timing_events_dq=None):
+             timing_events_dq=None, workspace_cleared=False):
     """dq, dk, dv (bf16, shaped like q, k, v but contiguous) and dsinks [Hq]
     fp32 (None when ``sinks`` is None). With ``accumulate_dsinks`` the sink
     gradient is added to the given ``dsinks`` instead of overwriting it. With
     ``deterministic`` dq is summed in a fixed order by a second,
     query-stationary pass, so every output is bit-identical from run to run;
-    ``timing_events_dq`` (two CUDA events) are recorded around that pass."""
+    ``timing_events_dq`` (two CUDA events) are recorded around that pass.
+    ``workspace_cleared``: the forward of this same problem was given this
+    ``workspace`` as its ``bwd_workspace`` and cleared the dq accumulator in
+    it (nothing may have written to it since), so the backward skips that."""
     _validate_inputs(q, k, v, sinks, cu_seqlens)
     for name, t in (("o", o), ("dout", dout)):
         _check_tokens(name, t, 1)
@@ -128,6 +136,7 @@ def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=Tru
     p.accumulate_dsinks = 1 if accumulate_dsinks else 0
     p.deterministic = 1 if deterministic else 0
     p.timing_events_dq[0], p.timing_events_dq[1] = _events(timing_events_dq)
+    p.workspace_cleared = 1 if workspace_cleared else 0
     check(L.sinkattn_bwd(ctypes.byref(p), _stream_ptr(q.device)), "sinkattn_bwd")
     return dq, dk, dv, dsinks
 
@@ -353,14 +362,16 @@ class HostPipeline:
                 self.s_run.wait_event(g["qkv"])
                 forward(q, k, v, self.sinks, g["cu"], g["max_seqlen"], causal=self.causal,
                         window=self.window, scale=self.scale, out=o, lse=g["lse"],
-                        workspace=self.ws_f)
+                        workspace=self.ws_f,
+                        bwd_workspace=None if self.deterministic else self.ws_b)
                 g["fwd"].record(self.s_run)
                 self.s_run.wait_event(g["do"])
                 backward(q, k, v, self.sinks, g["cu"], g["max_seqlen"], o, g["lse"], do,
                          causal=self.causal, window=self.window, scale=self.scale,
                          dq=self.dq[sl], dk=self.dk[sl], dv=self.dv[sl], dsinks=self.dsinks,
                          workspace=self.ws_b, accumulate_dsinks=i > 0,
-                         deterministic=self.deterministic)
+                         deterministic=self.deterministic,
+                         workspace_cleared=not self.deterministic)
                 g["bwd"].record(self.s_run)
         # outputs: a group's o as soon as its forward is done, then its gradients
         self.s_out.wait_stream(cur)

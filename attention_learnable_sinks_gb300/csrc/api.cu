@@ -300,6 +300,15 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
   int sms = 0;
   st = device_info(&p.err, &sms);
   if (st != SINKATTN_OK) return st;
+  if (a->bwd_workspace) {
+    // clear the backward's dq accumulator during the forward
+    const Layout lb = layout(a->nseq, a->total, a->Hq, true);
+    if (a->bwd_workspace_bytes < lb.bytes || !aligned16(a->bwd_workspace))
+      return fail(SINKATTN_ERR_WORKSPACE,
+                  "bwd_workspace smaller than sinkattn_bwd_workspace_size() or not 16-byte aligned");
+    p.clear = static_cast<uint8_t*>(a->bwd_workspace) + lb.dq_acc;
+    p.clear_bytes = (int64_t)(lb.bytes - lb.dq_acc);
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(a->workspace);
   TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
@@ -352,6 +361,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.dsinks = a->dsinks;
   bp.accumulate_dsinks = a->accumulate_dsinks != 0;
   bp.deterministic = a->deterministic != 0;
+  bp.acc_cleared = a->workspace_cleared != 0 && !bp.deterministic;
   bp.D = reinterpret_cast<float*>(ws + l.D);
   bp.sink_part = reinterpret_cast<float*>(ws + l.part);
   bp.dq_acc = reinterpret_cast<float*>(ws + l.dq_acc);

@@ -83,7 +83,7 @@ preprocess_kernel(BwdProblem bp) {
       const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(b2[e]);
       D = fmaf(x.x, y.x, fmaf(x.y, y.y, D));
     }
-    if (!bp.deterministic) {  // the atomic dq path sums into the accumulator
+    if (!bp.deterministic && !bp.acc_cleared) {  // the atomic dq path sums into the accumulator
       float4* acc = reinterpret_cast<float4*>(bp.dq_acc + row * kHeadDim) + sub * 2;
       acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);

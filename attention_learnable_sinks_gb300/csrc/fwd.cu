@@ -62,6 +62,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;  // log2 units
 constexpr int kSchedSlots = 4;
 constexpr int kSchedConsumers = 1 + 4;  // the UMMA warp and 4 softmax warps
+constexpr uint32_t kClearChunk = 4096;  // bytes of the backward's dq accumulator per copy
 
 // Training: base = the sequence's first token, r0 = the tile's first row,
 // nrows = rows in the tile, h = the query head. Decode: base = the sequence,
@@ -75,6 +76,7 @@ struct __align__(1024) Smem {
   uint8_t k[kKStages][kTileBytes];
   uint8_t v[kVStages][kTileBytes];
   uint8_t ostage[4][32 * 128];  // per softmax warp: its 32 rows of O (bf16), 16-byte chunks swizzled
+  uint8_t zeros[kClearChunk];   // source of the bulk copies that clear the backward's dq accumulator
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t q_full, q_empty, s_full, s_empty, p_full, o_done, drain;
@@ -153,6 +155,19 @@ __device__ __forceinline__ int next_unit(SmemT& sm, uint32_t& n, const Guard& g,
   return w;
 }
 
+// Bulk copy of shared memory to global memory (16-byte aligned, a multiple of
+// 16 bytes), in the thread's bulk group; commit_group / wait_group below.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Wait that ignores the abort flag (still time-bounded): used only to drain
 // copies / products this thread issued before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -203,6 +218,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     tma_prefetch(&tm_k);
     tma_prefetch(&tm_v);
   }
+  if (!kDecode && p.clear) {  // the zero source of the clearing copies
+    for (int i = threadIdx.x; i < (int)(kClearChunk / 16); i += kThreads)
+      reinterpret_cast<uint4*>(sm.zeros)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();
+  }
   __syncthreads();
   tc_fence_after();
   // broadcast so the compiler sees a warp-uniform value (UMMA operands)
@@ -213,6 +233,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t nq = 0, nk = 0, nv = 0;
+      // This CTA's share of the backward's dq accumulator, cleared one chunk
+      // per key-tile load (the forward leaves memory bandwidth unused) and the
+      // rest after its last unit.
+      int64_t clr = 0, clr_end = 0;
+      if (!kDecode && p.clear) {
+        const int64_t n16 = p.clear_bytes / 16;
+        clr = n16 * blockIdx.x / gridDim.x * 16;
+        clr_end = n16 * (blockIdx.x + 1) / gridDim.x * 16;
+      }
+      auto clear_some = [&]() {
+        if (clr < clr_end) {
+          const int64_t left = clr_end - clr;
+          const uint32_t n = left < (int64_t)kClearChunk ? (uint32_t)left : kClearChunk;
+          bulk_store(p.clear + clr, sm.zeros, n);
+          clr += n;
+        }
+      };
       // a key tile: one copy, or (decode) one per cache block; a block past
       // the sequence end or wholly before the window is read out of bounds,
       // which fills it with zeros
@@ -242,6 +279,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_expect_tx(&sm.k_full[s], kTileBytes);
         load_tile(sm.k[s], &tm_k, &sm.k_full[s], u, kt);
         ++nk;
+        clear_some();
         return true;
       };
       auto load_v = [&](const Unit& u, int kt) -> bool {
@@ -298,6 +336,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         if (!ok) break;
       }
+      if (!g.aborted())
+        while (clr < clr_end) clear_some();
+      bulk_wait_all();  // the clearing copies (this thread's own) are done
       if (g.aborted()) {  // let issued copies land before the CTA exits
         if (nq) drain_wait(&sm.q_full, (nq - 1) & 1);
         for (uint32_t c = nk > kKStages ? nk - kKStages : 0; c < nk; ++c)

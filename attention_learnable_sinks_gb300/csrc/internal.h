@@ -30,6 +30,8 @@ struct Problem {
   uint64_t wait_limit_ns;      // time limit of every wait inside the kernels
   int32_t withhold_copies;     // test hook: producers issue no copies (the
                                // consumers' waits run out)
+  uint8_t* clear;              // forward: bytes to clear for the backward (or null)
+  int64_t clear_bytes;         // a multiple of 16
 };
 
 struct BwdProblem {
@@ -48,6 +50,7 @@ struct BwdProblem {
   int32_t part_stride;         // key-tile capacity
   int32_t accumulate_dsinks;   // add to dsinks instead of overwriting it
   int32_t deterministic;       // dq from the query-stationary pass (no dq_acc)
+  int32_t acc_cleared;         // the forward cleared dq_acc: the preprocess skips it
 };
 
 // Decode over a paged KV cache, as the kernels see it.

@@ -338,13 +338,16 @@ def run_gb300(args):
     dq_ev = [new_events(2) for _ in range(K)] if det else None
 
     def step(i=None):
+        # the forward clears the backward's dq accumulator (atomic mode)
         api.forward(q, k, v, s, cu, maxlen, causal=w.causal, window=w.window, scale=w.scale,
                     out=o, lse=lse, workspace=ws_f,
-                    timing_events=None if i is None else fwd_ev[i])
+                    timing_events=None if i is None else fwd_ev[i],
+                    bwd_workspace=None if det else ws_b)
         api.backward(q, k, v, s, cu, maxlen, o, lse, do, causal=w.causal, window=w.window,
                      scale=w.scale, dq=dq, dk=dk, dv=dv, dsinks=ds, workspace=ws_b,
                      timing_events=None if i is None else bwd_ev[i], deterministic=det,
-                     timing_events_dq=None if i is None or not det else dq_ev[i])
+                     timing_events_dq=None if i is None or not det else dq_ev[i],
+                     workspace_cleared=not det)
         if world > 1:  # data parallel: sum the ranks' sink gradients
             sharding.all_reduce_sink_grad(ds)
 
@@ -595,7 +598,7 @@ def run_decode(args):
 
     def step():
         api.decode(q, kc, vc, table, lens, s, window=w.window, scale=w.scale, out=o, lse=lse,
-                   workspace=ws)
+                   workspace=ws, exact=args.decode_exact)
 
     for _ in range(args.warmup):
         step()
@@ -659,7 +662,10 @@ def run_decode(args):
         "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
-        "config": decode_config_record(w, args.workload),
+        "config": dict(decode_config_record(w, args.workload),
+                       decode=("exact: each row computed as the training forward's last row "
+                               "(bitwise equal), one unit per (sequence, kv head)")
+                       if args.decode_exact else "split keys + sink-aware combine"),
         "sequences_per_s": w.nseq * world * K / (total_ms / 1e3),
         "roofline": {"bound": "hbm", "kernel": "decode (split + combine)", "achieved": value / world,
                      "peak": hbm, "unit": "GB/s", "frac": value / world / hbm,
@@ -695,6 +701,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
                     help="backward with dq summed in a fixed order (query-stationary dq pass)")
+    ap.add_argument("--decode-exact", action="store_true",
+                    help="decode workloads: the exact decode (bitwise equal to the training "
+                         "forward's last row) instead of the split decode")
     ap.add_argument("--e2e-groups", type=int, default=2,
                     help="groups of whole sequences streamed by the end-to-end leg")
     args = ap.parse_args(argv)

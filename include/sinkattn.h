@@ -106,6 +106,16 @@ typedef struct sinkattn_fwd_params {
   int32_t causal;              /* 1 = causal mask, 0 = none                   */
   int32_t window;              /* <= 0: no window; W > 0 needs causal = 1     */
   float softmax_scale;         /* <= 0 selects 1/sqrt(head_dim)               */
+  void* bwd_workspace;         /* optional (NULL = none): the workspace the
+                                  backward of this same problem will use. The
+                                  forward then clears the fp32 dq accumulator
+                                  in it while it computes (it has memory
+                                  bandwidth to spare; the backward's first
+                                  pass does not), and that backward, called
+                                  with workspace_cleared = 1 and nothing
+                                  written to the workspace in between, skips
+                                  its own clear. Ignored by the backward.     */
+  size_t bwd_workspace_bytes;  /* >= sinkattn_bwd_workspace_size() when set    */
 } sinkattn_fwd_params;
 
 /* Backward: dq, dk, dv and dL/dS_h (same section, step 2). The forward fields
@@ -137,6 +147,11 @@ typedef struct sinkattn_bwd_params {
                                   run (dk, dv and dsinks always are).        */
   void* timing_events_dq[2];   /* optional, around the deterministic dq pass
                                   (ignored when deterministic = 0)           */
+  int32_t workspace_cleared;   /* nonzero: the forward of this same problem
+                                  cleared this workspace's dq accumulator
+                                  (fwd.bwd_workspace) and nothing has written
+                                  to the workspace since; the backward skips
+                                  that clear. Ignored when deterministic.    */
 } sinkattn_bwd_params;
 
 /* Workspace sizes in bytes for a problem of this shape (0 on bad input).

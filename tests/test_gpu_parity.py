@@ -11,7 +11,7 @@ import torch
 from attention_learnable_sinks_gb300 import _binding, api
 from attention_learnable_sinks_gb300.workloads import config, make
 
-from parity import (ALL, assert_dsinks, compare_full, dsink_condition, run_cuda,
+from parity import (ALL, assert_dsinks, compare_full, dsink_condition, f64, run_cuda,
                     run_oracle)
 
 pytestmark = pytest.mark.gpu
@@ -148,3 +148,30 @@ def test_rejects_bad_arguments_before_launch(cuda_lib):
         api.forward(q, k, v, None, cu, 64, causal=False, window=8)
     assert e.value.status == 2
     assert _binding.launch_count() == n0
+
+
+@pytest.mark.parametrize("case", [("dense_like", [1024, 1024], 16, 2, 0), ("ragged", [300, 77, 0, 129, 1], 8, 1, 0),
+                                  ("window", [700, 129], 8, 2, 128)], ids=lambda c: c[0])
+def test_forward_clears_backward_workspace(cuda_lib, case):
+    """The forward, given the backward's workspace, clears the dq accumulator
+    in it, and the backward told so skips its own clear. The workspace starts
+    full of garbage, so a byte the forward missed would show in dq."""
+    name, lengths, Hq, Hkv, window = case
+    w = make(name, lengths, Hq, Hkv, seed=61, window=window)
+    dev = "cuda"
+    q, k, v, do = (t.to(dev) for t in (w.q, w.k, w.v, w.dout))
+    s, cu = w.sinks.to(dev), w.cu_seqlens.to(dev)
+    ws_b = torch.empty(api.workspace_bytes("bwd", w.nseq, w.total, Hq, Hkv), dtype=torch.uint8,
+                       device=dev)
+    ref, *_ = run_oracle(w)
+    for fill in (0x7F, 0xA5):
+        ws_b.fill_(fill)
+        o, lse = api.forward(q, k, v, s, cu, w.max_seqlen, window=window, bwd_workspace=ws_b)
+        dq, dk, dv, ds = api.backward(q, k, v, s, cu, w.max_seqlen, o, lse, do, window=window,
+                                      workspace=ws_b, workspace_cleared=True)
+        torch.cuda.synchronize()
+        assert _binding.device_error(reset=True) == 0
+        got = {"o": f64(o), "lse": f64(lse), "dq": f64(dq), "dk": f64(dk), "dv": f64(dv)}
+        compare_full(w, got, ref)
+        cond = dsink_condition(w.sinks.numpy().astype(np.float64), ref["lse"], ref["o"], ref["_do"])
+        assert_dsinks(f64(ds), ref["dsinks"], cond)
