@@ -362,16 +362,14 @@ class HostPipeline:
                 self.s_run.wait_event(g["qkv"])
                 forward(q, k, v, self.sinks, g["cu"], g["max_seqlen"], causal=self.causal,
                         window=self.window, scale=self.scale, out=o, lse=g["lse"],
-                        workspace=self.ws_f,
-                        bwd_workspace=None if self.deterministic else self.ws_b)
+                        workspace=self.ws_f)
                 g["fwd"].record(self.s_run)
                 self.s_run.wait_event(g["do"])
                 backward(q, k, v, self.sinks, g["cu"], g["max_seqlen"], o, g["lse"], do,
                          causal=self.causal, window=self.window, scale=self.scale,
                          dq=self.dq[sl], dk=self.dk[sl], dv=self.dv[sl], dsinks=self.dsinks,
                          workspace=self.ws_b, accumulate_dsinks=i > 0,
-                         deterministic=self.deterministic,
-                         workspace_cleared=not self.deterministic)
+                         deterministic=self.deterministic)
                 g["bwd"].record(self.s_run)
         # outputs: a group's o as soon as its forward is done, then its gradients
         self.s_out.wait_stream(cur)

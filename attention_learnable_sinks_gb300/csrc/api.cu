@@ -82,6 +82,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // the order by cost.
 constexpr size_t kSeqMajorAccBytes = size_t(192) << 20;
 
+// Key tiles sequence by sequence when the fp32 dq accumulator is well beyond
+// L2 (the running units then share their sequences' rows of it).
+bool keys_seq_major(const Problem& p, bool deterministic) {
+  return !deterministic && p.nseq > 1 &&
+         (size_t)p.total * p.Hq * kHeadDim * sizeof(float) > kSeqMajorAccBytes;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Workspace layout. Forward: [meta | q-tile items]. Backward:
@@ -309,6 +316,14 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
     p.clear = static_cast<uint8_t*>(a->bwd_workspace) + lb.dq_acc;
     p.clear_bytes = (int64_t)(lb.bytes - lb.dq_acc);
   }
+  // ... and builds its key-tile list, in the same launch as its own list
+  TileList bkt{};
+  if (a->bwd_workspace) {
+    const Layout lb = layout(a->nseq, a->total, a->Hq, true);
+    char* bws = static_cast<char*>(a->bwd_workspace);
+    bkt = TileList{reinterpret_cast<int32_t*>(bws + lb.k_meta), reinterpret_cast<int2*>(bws + lb.k_items),
+                   lb.capacity};
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(a->workspace);
   TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
@@ -316,7 +331,8 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
   FwdLaunch fl;
   cudaError_t e = prepare_fwd(p, &fl);
   if (e != cudaSuccess) return cuda_fail(e, "forward tensor maps");
-  e = launch_build_tile_list(p, 0, 0, qt, s);
+  e = launch_build_tile_list(p, 0, 0, qt, s, a->bwd_workspace ? &bkt : nullptr,
+                             keys_seq_major(p, false) ? 1 : 0);
   if (e != cudaSuccess) return cuda_fail(e, "tile list");
   record(a->timing_events[0], s);
   e = launch_fwd(p, fl, qt, sms, s);
@@ -375,12 +391,11 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   cudaError_t e = prepare_bwd_main(bp, &bl);
   if (e == cudaSuccess && bp.deterministic) e = prepare_bwd_dq();
   if (e != cudaSuccess) return cuda_fail(e, "backward tensor maps");
-  // Key tiles sequence by sequence when the fp32 dq accumulator is well
-  // beyond L2 (the running units then share their sequences' rows of it).
-  const bool seq_major = !bp.deterministic && bp.f.nseq > 1 &&
-                         (size_t)bp.f.total * bp.f.Hq * kHeadDim * sizeof(float) > kSeqMajorAccBytes;
-  e = launch_build_tile_list(bp.f, 1, seq_major ? 1 : 0, kt, s);
-  if (e != cudaSuccess) return cuda_fail(e, "key-tile list");
+  // The key-tile list (unless the forward built it with the clear)
+  if (!bp.acc_cleared) {
+    e = launch_build_tile_list(bp.f, 1, keys_seq_major(bp.f, bp.deterministic) ? 1 : 0, kt, s);
+    if (e != cudaSuccess) return cuda_fail(e, "key-tile list");
+  }
   if (bp.deterministic) {
     e = launch_build_tile_list(bp.f, 0, 0, qt, s);
     if (e != cudaSuccess) return cuda_fail(e, "query-tile list");

@@ -130,9 +130,12 @@ cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int tota
 
 // Launchers (each returns the cudaGetLastError() of its launch).
 // seq_major: sequence by sequence, each by decreasing cost (else by decreasing
-// cost over the whole batch).
+// cost over the whole batch). keys (optional): a key-tile list to build in
+// the same launch, in order keys_seq_major (the backward's, built by the
+// forward).
 cudaError_t launch_build_tile_list(const Problem& p, int by_keys, int seq_major,
-                                   const TileList& list, cudaStream_t s);
+                                   const TileList& list, cudaStream_t s,
+                                   const TileList* keys = nullptr, int keys_seq_major = 0);
 // Tensor maps and kernel attributes are prepared before a call's first
 // launch, so that its kernels go out back to back (host-side preparation
 // between two launches would leave the GPU idle).

@@ -46,11 +46,23 @@ __device__ inline int bucket_of(int seq_major, int levels, int b, int cost) {
   return kBuckets - 1 - min(key, kBuckets - 1);
 }
 
+// One list to build: which tiles, in which order, where.
+struct ListJob {
+  int by_keys, seq_major, capacity;
+  int2* items;
+  int32_t* meta;
+};
+
+// One CTA per list (a forward can build the backward's key-tile list with its
+// own query-tile list, in the same launch).
 __global__ void __launch_bounds__(kThreads)
 build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int max_seqlen,
-                       int causal, int window, int by_keys, int seq_major, int capacity,
-                       int2* __restrict__ items, int32_t* __restrict__ meta,
+                       int causal, int window, ListJob job0, ListJob job1,
                        int32_t* __restrict__ err) {
+  const ListJob& job = blockIdx.x == 0 ? job0 : job1;
+  const int by_keys = job.by_keys, seq_major = job.seq_major, capacity = job.capacity;
+  int2* __restrict__ items = job.items;
+  int32_t* __restrict__ meta = job.meta;
   // cost levels per sequence in sequence-major order
   const int levels = seq_major ? max(1, kBuckets / max(nseq, 1)) : 1;
   __shared__ int hist[kBuckets];
@@ -150,10 +162,12 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
 }  // namespace
 
 cudaError_t launch_build_tile_list(const Problem& p, int by_keys, int seq_major,
-                                   const TileList& list, cudaStream_t s) {
-  build_tile_list_kernel<<<1, kThreads, 0, s>>>(p.cu, p.nseq, p.total, p.max_seqlen, p.causal,
-                                                p.window, by_keys, seq_major, list.capacity,
-                                                list.items, list.meta, p.err);
+                                   const TileList& list, cudaStream_t s, const TileList* keys,
+                                   int keys_seq_major) {
+  const ListJob a{by_keys, seq_major, list.capacity, list.items, list.meta};
+  const ListJob b = keys ? ListJob{1, keys_seq_major, keys->capacity, keys->items, keys->meta} : a;
+  build_tile_list_kernel<<<keys ? 2 : 1, kThreads, 0, s>>>(p.cu, p.nseq, p.total, p.max_seqlen,
+                                                           p.causal, p.window, a, b, p.err);
   note_launch();
   return cudaGetLastError();
 }

@@ -108,13 +108,15 @@ typedef struct sinkattn_fwd_params {
   float softmax_scale;         /* <= 0 selects 1/sqrt(head_dim)               */
   void* bwd_workspace;         /* optional (NULL = none): the workspace the
                                   backward of this same problem will use. The
-                                  forward then clears the fp32 dq accumulator
-                                  in it while it computes (it has memory
-                                  bandwidth to spare; the backward's first
-                                  pass does not), and that backward, called
-                                  with workspace_cleared = 1 and nothing
-                                  written to the workspace in between, skips
-                                  its own clear. Ignored by the backward.     */
+                                  forward then prepares it: clears the fp32 dq
+                                  accumulator in it while it computes (it has
+                                  memory bandwidth to spare; the backward's
+                                  first pass does not) and builds the
+                                  backward's key-tile list beside its own.
+                                  That backward, called with
+                                  workspace_cleared = 1 and nothing written to
+                                  the workspace in between, skips both.
+                                  Ignored by the backward.                   */
   size_t bwd_workspace_bytes;  /* >= sinkattn_bwd_workspace_size() when set    */
 } sinkattn_fwd_params;
 
@@ -148,10 +150,11 @@ typedef struct sinkattn_bwd_params {
   void* timing_events_dq[2];   /* optional, around the deterministic dq pass
                                   (ignored when deterministic = 0)           */
   int32_t workspace_cleared;   /* nonzero: the forward of this same problem
-                                  cleared this workspace's dq accumulator
-                                  (fwd.bwd_workspace) and nothing has written
-                                  to the workspace since; the backward skips
-                                  that clear. Ignored when deterministic.    */
+                                  prepared this workspace (fwd.bwd_workspace:
+                                  the dq accumulator cleared, the key-tile
+                                  list built) and nothing has written to it
+                                  since; the backward skips those steps.
+                                  Ignored when deterministic.                */
 } sinkattn_bwd_params;
 
 /* Workspace sizes in bytes for a problem of this shape (0 on bad input).
