@@ -13,7 +13,8 @@ import torch
 from . import _binding
 from ._binding import BwdParams, DecodeParams, FwdParams, check
 
-HEAD_DIM = 64
+HEAD_DIM = 64               # the head dim of decode, and the default
+HEAD_DIMS = (64, 128)       # head dims of forward and backward
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -34,11 +35,12 @@ def _events(evs) -> Sequence[Optional[int]]:
     return out
 
 
-def _check_tokens(name: str, t: torch.Tensor, heads_dim: int):
+def _check_tokens(name: str, t: torch.Tensor, head_dim: int):
     if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3:
-        raise ValueError(f"{name} must be a bf16 CUDA tensor [total, heads, 64]")
-    if t.shape[2] != HEAD_DIM or t.stride(2) != 1 or t.stride(1) != HEAD_DIM:
-        raise ValueError(f"{name}: heads and features must be contiguous (strides (*, 64, 1))")
+        raise ValueError(f"{name} must be a bf16 CUDA tensor [total, heads, head_dim]")
+    if t.shape[2] != head_dim or t.stride(2) != 1 or t.stride(1) != head_dim:
+        raise ValueError(f"{name}: must be [total, heads, {head_dim}] with heads and features "
+                         f"contiguous (strides (*, {head_dim}, 1))")
 
 
 def _fill_fwd(p: FwdParams, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale, o, lse):
@@ -58,11 +60,14 @@ def _fill_fwd(p: FwdParams, q, k, v, sinks, cu_seqlens, max_seqlen, causal, wind
 
 
 def _validate_inputs(q, k, v, sinks, cu_seqlens):
-    _check_tokens("q", q, 1)
-    _check_tokens("k", k, 1)
-    _check_tokens("v", v, 1)
+    if q.dim() != 3 or q.shape[2] not in HEAD_DIMS:
+        raise ValueError("q must be [total, Hq, head_dim] with head_dim 64 or 128")
+    d = q.shape[2]
+    _check_tokens("q", q, d)
+    _check_tokens("k", k, d)
+    _check_tokens("v", v, d)
     if k.shape != v.shape or k.shape[0] != q.shape[0]:
-        raise ValueError("k and v must be [total, Hkv, 64] with the same total as q")
+        raise ValueError("k and v must be [total, Hkv, head_dim] with the same total and head_dim as q")
     if sinks is not None and (sinks.dtype != torch.float32 or not sinks.is_cuda or
                               sinks.shape != (q.shape[1],) or not sinks.is_contiguous()):
         raise ValueError("sinks must be a contiguous fp32 CUDA tensor [Hq]")
@@ -72,10 +77,12 @@ def _validate_inputs(q, k, v, sinks, cu_seqlens):
 
 def forward(q, k, v, sinks, cu_seqlens, max_seqlen, *, causal=True, window=0, scale=None,
             out=None, lse=None, workspace=None, timing_events=None, bwd_workspace=None):
-    """O [total, Hq, 64] bf16 and LSE [Hq, total] fp32 (natural log). With
-    ``bwd_workspace`` (the workspace the backward of this same problem will
-    use) the forward also clears the backward's dq accumulator in it; pass
-    ``workspace_cleared=True`` to that backward."""
+    """O [total, Hq, d] bf16 and LSE [Hq, total] fp32 (natural log), d = 64 or
+    128. With ``bwd_workspace`` (the workspace the backward of this same
+    problem will use; head_dim 64) the forward also prepares it: it clears the
+    backward's dq accumulator and builds its key-tile list; pass
+    ``workspace_cleared=True`` to that backward. At head_dim 128 it is not
+    used."""
     _validate_inputs(q, k, v, sinks, cu_seqlens)
     L = _binding.lib()
     total, Hq, d = q.shape
@@ -105,12 +112,13 @@ def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=Tru
     ``deterministic`` dq is summed in a fixed order by a second,
     query-stationary pass, so every output is bit-identical from run to run;
     ``timing_events_dq`` (two CUDA events) are recorded around that pass.
+    At head_dim 128 the backward always works this way.
     ``workspace_cleared``: the forward of this same problem was given this
     ``workspace`` as its ``bwd_workspace`` and cleared the dq accumulator in
     it (nothing may have written to it since), so the backward skips that."""
     _validate_inputs(q, k, v, sinks, cu_seqlens)
     for name, t in (("o", o), ("dout", dout)):
-        _check_tokens(name, t, 1)
+        _check_tokens(name, t, q.shape[2])
         if not t.is_contiguous() or t.shape != q.shape:
             raise ValueError(f"{name} must be contiguous and shaped like q")
     L = _binding.lib()
@@ -193,13 +201,14 @@ def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, s
 
 
 def workspace_bytes(kind: str, nseq: int, total: int, Hq: int, Hkv: int,
-                    deterministic: bool = False) -> int:
+                    deterministic: bool = False, head_dim: int = HEAD_DIM) -> int:
     """Workspace bytes of the forward ("fwd") or of the backward ("bwd") in the
-    given mode (the deterministic backward needs no fp32 dq accumulator)."""
+    given mode (the deterministic backward, which head_dim 128 always uses,
+    needs no fp32 dq accumulator)."""
     L = _binding.lib()
     if kind == "fwd":
-        return int(L.sinkattn_fwd_workspace_size(nseq, total, Hq, Hkv, HEAD_DIM))
-    return int(L.sinkattn_bwd_workspace_size_mode(nseq, total, Hq, Hkv, HEAD_DIM,
+        return int(L.sinkattn_fwd_workspace_size(nseq, total, Hq, Hkv, head_dim))
+    return int(L.sinkattn_bwd_workspace_size_mode(nseq, total, Hq, Hkv, head_dim,
                                                   1 if deterministic else 0))
 
 
@@ -226,9 +235,10 @@ def sink_attention(q, k, v, sinks=None, cu_seqlens=None, max_seqlen=None, *, cau
                    window=0, scale=None, deterministic=False):
     """Attention with one learnable sink logit per query head.
 
-    q [total, Hq, 64], k/v [total, Hkv, 64] bf16 with cu_seqlens (int32
-    [nseq+1]) for packed variable-length batches, or q [B, T, Hq, 64],
-    k/v [B, T, Hkv, 64] for a dense batch. sinks: fp32 [Hq] or None.
+    q [total, Hq, d], k/v [total, Hkv, d] bf16 (d = 64 or 128) with
+    cu_seqlens (int32 [nseq+1]) for packed variable-length batches, or
+    q [B, T, Hq, d], k/v [B, T, Hkv, d] for a dense batch. sinks: fp32 [Hq]
+    or None.
     Returns O shaped like q. Differentiable in q, k, v and sinks; with
     ``deterministic`` the backward is bit-identical from run to run.
     """
@@ -286,7 +296,7 @@ class HostPipeline:
     """
 
     def __init__(self, cu_seqlens, Hq: int, Hkv: int, *, causal=True, window=0, scale=None,
-                 groups: int = 2, device=None, deterministic=False):
+                 groups: int = 2, device=None, deterministic=False, head_dim: int = HEAD_DIM):
         device = torch.device(device if device is not None else "cuda")
         cu = [int(x) for x in cu_seqlens.tolist()]
         lens = [b - a for a, b in zip(cu[:-1], cu[1:])]
@@ -295,7 +305,7 @@ class HostPipeline:
         self.deterministic = deterministic
         self.Hq, self.Hkv, self.total = Hq, Hkv, cu[-1]
         self.device = device
-        d = HEAD_DIM
+        self.head_dim = d = head_dim
         bf = dict(dtype=torch.bfloat16, device=device)
         self.q = torch.empty(self.total, Hq, d, **bf)
         self.k = torch.empty(self.total, Hkv, d, **bf)
@@ -320,8 +330,8 @@ class HostPipeline:
                 "qkv": torch.cuda.Event(), "do": torch.cuda.Event(),
                 "fwd": torch.cuda.Event(), "bwd": torch.cuda.Event(),
             })
-            fw = max(fw, workspace_bytes("fwd", b - a, t1 - t0, Hq, Hkv))
-            bw = max(bw, workspace_bytes("bwd", b - a, t1 - t0, Hq, Hkv))
+            fw = max(fw, workspace_bytes("fwd", b - a, t1 - t0, Hq, Hkv, head_dim=d))
+            bw = max(bw, workspace_bytes("bwd", b - a, t1 - t0, Hq, Hkv, head_dim=d))
         self.ws_f = torch.empty(fw, dtype=torch.uint8, device=device)
         self.ws_b = torch.empty(bw, dtype=torch.uint8, device=device)
         self.s_in = torch.cuda.Stream(device)
@@ -329,11 +339,11 @@ class HostPipeline:
         self.s_out = torch.cuda.Stream(device)
 
     def h2d_bytes(self) -> int:
-        per_tok = (2 * self.Hq + 2 * self.Hkv) * HEAD_DIM * 2
+        per_tok = (2 * self.Hq + 2 * self.Hkv) * self.head_dim * 2
         return self.total * per_tok + 4 * self.Hq + sum(4 * g["cu"].numel() for g in self.groups)
 
     def d2h_bytes(self) -> int:
-        return self.total * (2 * self.Hq + 2 * self.Hkv) * HEAD_DIM * 2 + 4 * self.Hq
+        return self.total * (2 * self.Hq + 2 * self.Hkv) * self.head_dim * 2 + 4 * self.Hq
 
     def run(self, hq, hk, hv, hdout, hsinks, ho, hdq, hdk, hdv, hdsinks):
         """Enqueue the whole batch: host inputs (pinned, shaped like the device

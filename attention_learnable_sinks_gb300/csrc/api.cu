@@ -85,7 +85,7 @@ constexpr size_t kSeqMajorAccBytes = size_t(192) << 20;
 // Key tiles sequence by sequence when the fp32 dq accumulator is well beyond
 // L2 (the running units then share their sequences' rows of it).
 bool keys_seq_major(const Problem& p, bool deterministic) {
-  return !deterministic && p.nseq > 1 &&
+  return !deterministic && p.head_dim == kHeadDim && p.nseq > 1 &&
          (size_t)p.total * p.Hq * kHeadDim * sizeof(float) > kSeqMajorAccBytes;
 }
 
@@ -135,11 +135,20 @@ bool shape_ok(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv) {
   return nseq >= 0 && total >= 0 && Hq > 0 && Hkv > 0 && Hq % Hkv == 0 && Hq <= 65535;
 }
 
+bool head_dim_ok(int32_t d) { return d == kHeadDim || d == kHeadDimWide; }
+
+// The backward at head_dim 128 always takes dq from the query-stationary pass:
+// tensor memory holds dK and dV (256 columns) and the S^T / dP^T buffers, with
+// no room left for a dQ accumulator.
+bool bwd_deterministic(int32_t head_dim, int32_t deterministic) {
+  return deterministic != 0 || head_dim != kHeadDim;
+}
+
 // Checks shared by forward and backward; fills the kernels' view.
 sinkattn_status check_fwd(const sinkattn_fwd_params* a, Problem* p) {
   if (!a) return fail(SINKATTN_ERR_INVALID_ARG, "params is NULL");
-  if (a->head_dim != kHeadDim)
-    return fail(SINKATTN_ERR_UNSUPPORTED, "head_dim must be 64");
+  if (!head_dim_ok(a->head_dim))
+    return fail(SINKATTN_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (!shape_ok(a->nseq, a->total, a->Hq, a->Hkv))
     return fail(SINKATTN_ERR_INVALID_ARG, "need nseq >= 0, total >= 0, 0 < Hkv, Hq % Hkv == 0, Hq <= 65535");
   if (a->causal != 0 && a->causal != 1) return fail(SINKATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
@@ -150,10 +159,11 @@ sinkattn_status check_fwd(const sinkattn_fwd_params* a, Problem* p) {
   if (!a->cu_seqlens) return fail(SINKATTN_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (std::isnan(a->softmax_scale) || std::isinf(a->softmax_scale))
     return fail(SINKATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
-  const int64_t qs = a->q_row_stride ? a->q_row_stride : (int64_t)a->Hq * kHeadDim;
-  const int64_t ks = a->k_row_stride ? a->k_row_stride : (int64_t)a->Hkv * kHeadDim;
-  const int64_t vs = a->v_row_stride ? a->v_row_stride : (int64_t)a->Hkv * kHeadDim;
-  if (qs < (int64_t)a->Hq * kHeadDim || ks < (int64_t)a->Hkv * kHeadDim || vs < (int64_t)a->Hkv * kHeadDim ||
+  const int64_t d = a->head_dim;
+  const int64_t qs = a->q_row_stride ? a->q_row_stride : (int64_t)a->Hq * d;
+  const int64_t ks = a->k_row_stride ? a->k_row_stride : (int64_t)a->Hkv * d;
+  const int64_t vs = a->v_row_stride ? a->v_row_stride : (int64_t)a->Hkv * d;
+  if (qs < (int64_t)a->Hq * d || ks < (int64_t)a->Hkv * d || vs < (int64_t)a->Hkv * d ||
       qs % 8 || ks % 8 || vs % 8)
     return fail(SINKATTN_ERR_INVALID_ARG, "row strides must cover all heads and be multiples of 8 elements");
   if (a->total > 0) {
@@ -179,9 +189,10 @@ sinkattn_status check_fwd(const sinkattn_fwd_params* a, Problem* p) {
   p->Hkv = a->Hkv;
   p->G = a->Hq / a->Hkv;
   p->causal = a->causal;
+  p->head_dim = a->head_dim;
   // a window at least as long as every sequence restricts nothing
   p->window = (a->window > 0 && a->window < a->max_seqlen) ? a->window : 0;
-  p->scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+  p->scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)a->head_dim);
   p->scale_log2 = p->scale * 1.4426950408889634f;
   p->wait_limit_ns = wait_limit_ns();
   p->withhold_copies = withhold_copies();
@@ -227,12 +238,12 @@ void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_re
 void note_error_message(const std::string& msg) { g_message = msg; }
 
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
-                                int64_t row_stride, int box_rows) {
+                                int64_t row_stride, int box_rows, int head_dim) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)total};
-  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)row_stride * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)box_rows};
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)total};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)row_stride * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   const cuuint32_t elem[3] = {1, 1, 1};
   // a box row is 128 bytes, one head of one token; promoting the L2 fill to
   // 256 bytes would also fetch the neighbouring head's row (measured 12%
@@ -280,7 +291,7 @@ extern "C" {
 
 size_t sinkattn_fwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
                                    int32_t head_dim) {
-  if (!shape_ok(nseq, total, Hq, Hkv) || head_dim != kHeadDim) return 0;
+  if (!shape_ok(nseq, total, Hq, Hkv) || !head_dim_ok(head_dim)) return 0;
   return layout(nseq, total, Hq, false).bytes;
 }
 
@@ -291,8 +302,8 @@ size_t sinkattn_bwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int3
 
 size_t sinkattn_bwd_workspace_size_mode(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
                                         int32_t head_dim, int32_t deterministic) {
-  if (!shape_ok(nseq, total, Hq, Hkv) || head_dim != kHeadDim) return 0;
-  return layout(nseq, total, Hq, true).bytes_for(deterministic != 0);
+  if (!shape_ok(nseq, total, Hq, Hkv) || !head_dim_ok(head_dim)) return 0;
+  return layout(nseq, total, Hq, true).bytes_for(bwd_deterministic(head_dim, deterministic));
 }
 
 sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
@@ -307,7 +318,10 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
   int sms = 0;
   st = device_info(&p.err, &sms);
   if (st != SINKATTN_OK) return st;
-  if (a->bwd_workspace) {
+  // head_dim 64: prepare the backward's workspace (at 128 the backward has no
+  // dq accumulator and builds its own lists: bwd_workspace is not used)
+  const bool prep = a->bwd_workspace && p.head_dim == kHeadDim;
+  if (prep) {
     // clear the backward's dq accumulator during the forward
     const Layout lb = layout(a->nseq, a->total, a->Hq, true);
     if (a->bwd_workspace_bytes < lb.bytes || !aligned16(a->bwd_workspace))
@@ -318,7 +332,7 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
   }
   // ... and builds its key-tile list, in the same launch as its own list
   TileList bkt{};
-  if (a->bwd_workspace) {
+  if (prep) {
     const Layout lb = layout(a->nseq, a->total, a->Hq, true);
     char* bws = static_cast<char*>(a->bwd_workspace);
     bkt = TileList{reinterpret_cast<int32_t*>(bws + lb.k_meta), reinterpret_cast<int2*>(bws + lb.k_items),
@@ -331,7 +345,7 @@ sinkattn_status sinkattn_fwd(const sinkattn_fwd_params* a, void* stream) {
   FwdLaunch fl;
   cudaError_t e = prepare_fwd(p, &fl);
   if (e != cudaSuccess) return cuda_fail(e, "forward tensor maps");
-  e = launch_build_tile_list(p, 0, 0, qt, s, a->bwd_workspace ? &bkt : nullptr,
+  e = launch_build_tile_list(p, 0, 0, qt, s, prep ? &bkt : nullptr,
                              keys_seq_major(p, false) ? 1 : 0);
   if (e != cudaSuccess) return cuda_fail(e, "tile list");
   record(a->timing_events[0], s);
@@ -355,7 +369,8 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
       return fail(SINKATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   }
   const Layout l = layout(f.nseq, f.total, f.Hq, true);
-  if (!a->workspace || a->workspace_bytes < l.bytes_for(a->deterministic != 0))
+  const bool det = bwd_deterministic(f.head_dim, a->deterministic);
+  if (!a->workspace || a->workspace_bytes < l.bytes_for(det))
     return fail(SINKATTN_ERR_WORKSPACE,
                 "workspace missing or smaller than sinkattn_bwd_workspace_size_mode()");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -376,7 +391,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   bp.dv = static_cast<__nv_bfloat16*>(a->dv);
   bp.dsinks = a->dsinks;
   bp.accumulate_dsinks = a->accumulate_dsinks != 0;
-  bp.deterministic = a->deterministic != 0;
+  bp.deterministic = det;
   bp.acc_cleared = a->workspace_cleared != 0 && !bp.deterministic;
   bp.D = reinterpret_cast<float*>(ws + l.D);
   bp.sink_part = reinterpret_cast<float*>(ws + l.part);
@@ -387,9 +402,12 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
               l.capacity};
   TileList qt{reinterpret_cast<int32_t*>(ws + l.q_meta), reinterpret_cast<int2*>(ws + l.q_items),
               l.capacity};
+  const bool wide = f.head_dim == kHeadDimWide;
   BwdLaunch bl;
+  BwdWideLaunch wl;
   cudaError_t e = prepare_bwd_main(bp, &bl);
-  if (e == cudaSuccess && bp.deterministic) e = prepare_bwd_dq();
+  if (e == cudaSuccess && wide) e = prepare_bwd_wide(bp, &wl);
+  if (e == cudaSuccess && bp.deterministic) e = prepare_bwd_dq(f.head_dim);
   if (e != cudaSuccess) return cuda_fail(e, "backward tensor maps");
   // The key-tile list (unless the forward built it with the clear)
   if (!bp.acc_cleared) {
@@ -403,7 +421,7 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
   e = launch_bwd_preprocess(bp, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess");
   record(a->timing_events[0], s);
-  e = launch_bwd_main(bp, bl, kt, sms, s);
+  e = wide ? launch_bwd_wide(bp, wl, kt, sms, s) : launch_bwd_main(bp, bl, kt, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward main");
   record(a->timing_events[1], s);
   if (bp.deterministic) {

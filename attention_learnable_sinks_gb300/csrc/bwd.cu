@@ -61,21 +61,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kPrepThreads = 256;
 
 // ---------------------------------------------------------------- preprocess
-// One warp per four (token, head) rows, 16 bytes per lane: D = rowsum(dO * O)
-// reduced over the row's eight lanes, and the row's 256 bytes of the fp32 dq
-// accumulator cleared with coalesced stores.
+// One warp per four (token, head) rows at head_dim 64 (two at 128), 16 bytes
+// per lane: D = rowsum(dO * O) reduced over the row's lanes, and (head_dim 64,
+// atomic dq) the row's 256 bytes of the fp32 dq accumulator cleared with
+// coalesced stores.
+template <int kD>
 __global__ void __launch_bounds__(kPrepThreads)
 preprocess_kernel(BwdProblem bp) {
+  constexpr int kLanes = kD / 8;  // lanes per row
   const Problem& p = bp.f;
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = ((int64_t)blockIdx.x * kPrepThreads + threadIdx.x) >> 5;
-  const int64_t row = warp_id * 4 + (lane >> 3);  // token * Hq + head
-  const int sub = lane & 7;                       // 16-byte chunk of the row
+  const int64_t row = warp_id * (32 / kLanes) + lane / kLanes;  // token * Hq + head
+  const int sub = lane % kLanes;                                // 16-byte chunk of the row
   const bool in = row < (int64_t)p.total * p.Hq;
   float D = 0.f;
   if (in) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p.o + row * kHeadDim + sub * 8);
-    const uint4 b = *reinterpret_cast<const uint4*>(bp.dout + row * kHeadDim + sub * 8);
+    const uint4 a = *reinterpret_cast<const uint4*>(p.o + row * kD + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(bp.dout + row * kD + sub * 8);
     const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
@@ -83,7 +86,7 @@ preprocess_kernel(BwdProblem bp) {
       const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(b2[e]);
       D = fmaf(x.x, y.x, fmaf(x.y, y.y, D));
     }
-    if (!bp.deterministic && !bp.acc_cleared) {  // the atomic dq path sums into the accumulator
+    if (kD == kHeadDim && !bp.deterministic && !bp.acc_cleared) {  // the atomic dq path sums into the accumulator
       float4* acc = reinterpret_cast<float4*>(bp.dq_acc + row * kHeadDim) + sub * 2;
       acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -95,9 +98,8 @@ preprocess_kernel(BwdProblem bp) {
          e += (int64_t)gridDim.x * kPrepThreads)
       bp.sink_part[e] = 0.f;
   }
-  D += __shfl_xor_sync(0xffffffffu, D, 1);
-  D += __shfl_xor_sync(0xffffffffu, D, 2);
-  D += __shfl_xor_sync(0xffffffffu, D, 4);
+#pragma unroll
+  for (int o = 1; o < kLanes; o <<= 1) D += __shfl_xor_sync(0xffffffffu, D, o);
   if (in && sub == 0) bp.D[(row % p.Hq) * p.total + row / p.Hq] = D;
 }
 
@@ -764,20 +766,26 @@ finish_kernel(BwdProblem bp) {
 cudaError_t launch_bwd_preprocess(const BwdProblem& p, cudaStream_t s) {
   const int64_t rows = (int64_t)p.f.total * p.f.Hq;
   if (rows == 0) return cudaSuccess;
-  const int64_t rows_per_block = kPrepThreads / 8;  // four rows per warp
-  preprocess_kernel<<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), kPrepThreads, 0,
-                      s>>>(p);
+  const int64_t rows_per_block = kPrepThreads * 8 / p.f.head_dim;  // lanes per row: head_dim / 8
+  const unsigned blocks = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
+  if (p.f.head_dim == kHeadDimWide)
+    preprocess_kernel<kHeadDimWide><<<blocks, kPrepThreads, 0, s>>>(p);
+  else
+    preprocess_kernel<kHeadDim><<<blocks, kPrepThreads, 0, s>>>(p);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l) {
-  cudaError_t e = make_tmap_bf16_rows(&l->q, p.f.q, p.f.Hq, p.f.total, p.f.q_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.f.k, p.f.Hkv, p.f.total, p.f.k_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.f.v, p.f.Hkv, p.f.total, p.f.v_stride);
+  // the Q / K / V / dO maps also serve the deterministic dq pass (any head dim)
+  const int d = p.f.head_dim;
+  cudaError_t e = make_tmap_bf16_rows(&l->q, p.f.q, p.f.Hq, p.f.total, p.f.q_stride, kTile, d);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.f.k, p.f.Hkv, p.f.total, p.f.k_stride, kTile, d);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.f.v, p.f.Hkv, p.f.total, p.f.v_stride, kTile, d);
   if (e == cudaSuccess)
-    e = make_tmap_bf16_rows(&l->dout, p.dout, p.f.Hq, p.f.total, (int64_t)p.f.Hq * kHeadDim);
-  if (e == cudaSuccess) e = make_tmap_f32_rows(&l->dq, p.dq_acc, p.f.Hq, p.f.total);
+    e = make_tmap_bf16_rows(&l->dout, p.dout, p.f.Hq, p.f.total, (int64_t)p.f.Hq * d, kTile, d);
+  if (e != cudaSuccess || d != kHeadDim) return e;
+  e = make_tmap_f32_rows(&l->dq, p.dq_acc, p.f.Hq, p.f.total);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(p.deterministic ? bwd_kernel<false> : bwd_kernel<true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

@@ -25,7 +25,13 @@
 // key tile are computed while it forms dS.
 // Tensor memory (512 columns): S [0,128), dP [128,256), dS [256,384) as two
 // 64-column bf16-pair buffers (by key tile), dQ [384,512) as two 64-column
-// buffers (by unit, so one unit's epilogue overlaps the next unit's products).
+// buffers at head_dim 64 (by unit, so one unit's epilogue overlaps the next
+// unit's products), one 128-column buffer at head_dim 128.
+//
+// Head_dim 128: the tiles are two 64-feature panels of 128-byte rows each (a
+// product over the features walks both); Q / dO have one buffer and K / V two
+// stages (192 KB of shared memory), so a unit's Q / dO load waits until the
+// previous unit's last S / dP have completed.
 #include <algorithm>
 #include <cmath>
 
@@ -38,9 +44,16 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 320;
-constexpr int kKVStages = 3;
-constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB of bf16
+constexpr uint32_t kPanelBytes = kTile * 64 * 2;  // 128 rows x 64 features of bf16
 constexpr uint32_t kTmemCols = 512;
+template <int kD>
+struct Cfg {
+  static constexpr int kPanels = kD / 64;
+  static constexpr uint32_t kTileBytes = kPanelBytes * kPanels;
+  static constexpr int kQBufs = kD == 64 ? 2 : 1;      // Q / dO buffers (by unit)
+  static constexpr int kKVStages = kD == 64 ? 3 : 2;   // K / V ring
+  static constexpr int kDQBufs = kD == 64 ? 2 : 1;     // dQ accumulators (by unit)
+};
 constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 384;  // + 64 per buffer
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSchedSlots = 4;
@@ -51,21 +64,28 @@ struct Unit {
   int base, L, r0, nrows, h, kvh, kt0, kt1;
 };
 
+template <int kD>
 struct __align__(1024) Smem {
-  uint8_t q[2][kTileBytes];
-  uint8_t dout[2][kTileBytes];
+  static constexpr uint32_t kTileBytes = Cfg<kD>::kTileBytes;
+  static constexpr int kQBufs = Cfg<kD>::kQBufs, kKVStages = Cfg<kD>::kKVStages;
+  uint8_t q[kQBufs][kTileBytes];
+  uint8_t dout[kQBufs][kTileBytes];
   uint8_t k[kKVStages][kTileBytes];
   uint8_t v[kKVStages][kTileBytes];
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kQBufs], q_empty[kQBufs];
   uint64_t kv_full[kKVStages], kv_empty[kKVStages];
-  uint64_t sdp_full, sdp_empty, ds_full[2], ds_free[2], dq_full[2], dq_empty[2], drain;
+  uint64_t sdp_full, sdp_empty, ds_full[2], ds_free[2];
+  uint64_t dq_full[Cfg<kD>::kDQBufs], dq_empty[Cfg<kD>::kDQBufs], drain;
   uint64_t sched_full[kSchedSlots], sched_empty[kSchedSlots];
   int32_t sched_unit[kSchedSlots];  // work unit handed out, -1 = no more work
   Unit sched_u[kSchedSlots];         // ... decoded by the producer
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+template <int kD>
+constexpr size_t smem_bytes() {
+  return sizeof(Smem<kD>) + 1024;
+}
 
 __device__ __forceinline__ Unit decode(const Problem& p, const int2* items, int w) {
   const int2 it = items[w / p.Hq];
@@ -92,23 +112,31 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (global_ns() - t0 > kWaitLimitNs) break;
 }
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
           BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__ meta) {
+  using C = Cfg<kD>;
+  constexpr uint32_t kTileBytes = C::kTileBytes;
+  constexpr int kQBufs = C::kQBufs, kKVStages = C::kKVStages, kDQBufs = C::kDQBufs;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
+  Smem<kD>& sm = *reinterpret_cast<Smem<kD>*>(smem_raw + align1024_pad(smem_raw));
   const Problem& p = bp.f;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Guard g{&sm.abort, p.err, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQBufs; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.ds_full[s], kSoftmaxThreads);
       mbar_init(&sm.ds_free[s], 1);
+    }
+    for (int s = 0; s < kDQBufs; ++s) {
       mbar_init(&sm.dq_full[s], 1);
       mbar_init(&sm.dq_empty[s], kSoftmaxThreads);
     }
@@ -159,11 +187,14 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         ++nsched;
         if (w < 0) break;
         if (p.withhold_copies) break;  // test hook: the consumers' waits run out
-        const int qb = nq & 1;
-        if (!mbar_wait(&sm.q_empty[qb], ((nq >> 1) & 1) ^ 1, g)) break;
+        const int qb = nq % kQBufs;
+        if (!mbar_wait(&sm.q_empty[qb], ((nq / kQBufs) & 1) ^ 1, g)) break;
         mbar_expect_tx(&sm.q_full[qb], 2 * kTileBytes);
-        tma_load_3d(sm.q[qb], &tm_q, &sm.q_full[qb], 0, u.h, u.base + u.r0);
-        tma_load_3d(sm.dout[qb], &tm_do, &sm.q_full[qb], 0, u.h, u.base + u.r0);
+#pragma unroll
+        for (int pi = 0; pi < C::kPanels; ++pi) {
+          tma_load_3d(sm.q[qb] + pi * kPanelBytes, &tm_q, &sm.q_full[qb], 64 * pi, u.h, u.base + u.r0);
+          tma_load_3d(sm.dout[qb] + pi * kPanelBytes, &tm_do, &sm.q_full[qb], 64 * pi, u.h, u.base + u.r0);
+        }
         ++nq;
         bool ok = true;
         for (int kt = u.kt0; kt < u.kt1 && ok; ++kt) {
@@ -173,15 +204,18 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
             break;
           }
           mbar_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
-          tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, u.kvh, u.base + kt * kTile);
-          tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], 0, u.kvh, u.base + kt * kTile);
+#pragma unroll
+          for (int pi = 0; pi < C::kPanels; ++pi) {
+            tma_load_3d(sm.k[st] + pi * kPanelBytes, &tm_k, &sm.kv_full[st], 64 * pi, u.kvh, u.base + kt * kTile);
+            tma_load_3d(sm.v[st] + pi * kPanelBytes, &tm_v, &sm.kv_full[st], 64 * pi, u.kvh, u.base + kt * kTile);
+          }
           ++nkv;
         }
         if (!ok) break;
       }
       if (g.aborted()) {  // let issued copies land before the CTA exits
-        for (uint32_t c = nq > 2 ? nq - 2 : 0; c < nq; ++c)
-          drain_wait(&sm.q_full[c & 1], (c >> 1) & 1);
+        for (uint32_t c = nq > (uint32_t)kQBufs ? nq - kQBufs : 0; c < nq; ++c)
+          drain_wait(&sm.q_full[c % kQBufs], (c / kQBufs) & 1);
         for (uint32_t c = nkv > kKVStages ? nkv - kKVStages : 0; c < nkv; ++c)
           drain_wait(&sm.kv_full[c % kKVStages], (c / kKVStages) & 1);
       }
@@ -191,12 +225,13 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // The whole warp runs this loop (uniform control flow and operands); one
     // elected lane issues each product and commit.
     const uint32_t idS = idesc_bf16(kTile, kTile, false, false);
-    const uint32_t idQ = idesc_bf16(kTile, kHeadDim, false, true);
+    const uint32_t idQ = idesc_bf16(kTile, kD, false, true);
     // descriptors built once; a product adds its byte offset / 16
     const uint64_t dQ0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
     const uint64_t dO0 = sdesc_sw128(smem_u32(sm.dout[0]), 16, 1024);
     const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);       // K-major
-    const uint64_t dKmn0 = sdesc_sw128(smem_u32(sm.k[0]), 8192, 1024);   // MN-major
+    // MN-major: the 64-feature panels are kPanelBytes apart
+    const uint64_t dKmn0 = sdesc_sw128(smem_u32(sm.k[0]), kPanelBytes, 1024);
     const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
     constexpr uint64_t kStageStep = kTileBytes >> 4;  // between stages of one array
     uint32_t nq = 0, nsdp = 0, nds = 0, nsched = 0;
@@ -213,9 +248,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       const uint64_t aq = dQ0 + qb * kStageStep, ao = dO0 + qb * kStageStep;
       const uint64_t bk = dK0 + st * kStageStep, bv = dV0 + st * kStageStep;
 #pragma unroll
-      for (int k = 0; k < kHeadDim / 16; ++k) {  // +32 bytes per 16 features
-        umma_ss_warp(tmem + kColS, aq + 2 * k, bk + 2 * k, idS, k > 0);
-        umma_ss_warp(tmem + kColDP, ao + 2 * k, bv + 2 * k, idS, k > 0);
+      for (int k = 0; k < kD / 16; ++k) {  // +32 bytes per 16 features, panel by panel
+        const uint64_t off = (uint64_t)(k / 4) * (kPanelBytes >> 4) + 2 * (k % 4);
+        umma_ss_warp(tmem + kColS, aq + off, bk + off, idS, k > 0);
+        umma_ss_warp(tmem + kColDP, ao + off, bv + off, idS, k > 0);
       }
       umma_commit_warp(&sm.sdp_full);
       return true;
@@ -225,7 +261,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // before dQ of the current one, so that a unit boundary leaves no gap in
     // the tensor pipe. fetch() returns 1 with the index of the next unit that
     // has key tiles (its Q / dO stage and dQ buffer are index % 2), 0 at the
-    // end of the work, -1 on abort.
+    // end of the work, -1 on abort.  (Buffers: Q / dO index % kQBufs, dQ
+    // index % kDQBufs.)
     auto fetch = [&](int& n, uint32_t& u) -> int {
       for (;;) {
         const int slot = nsched % kSchedSlots;
@@ -237,12 +274,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (lane == 0) mbar_arrive(&sm.sched_empty[slot]);
         if (w < 0) return 0;
         u = nq++;
-        if (!mbar_wait_warp(&sm.q_full[u & 1], (u >> 1) & 1, g)) return -1;
+        if (!mbar_wait_warp(&sm.q_full[u % kQBufs], (u / kQBufs) & 1, g)) return -1;
         if (n > 0) return 1;
         // no key tile: nothing reads Q / dO, and dq is written as zero
-        if (!mbar_wait_warp(&sm.dq_empty[u & 1], ((u >> 1) & 1) ^ 1, g)) return -1;
-        umma_commit_warp(&sm.q_empty[u & 1]);
-        umma_commit_warp(&sm.dq_full[u & 1]);
+        if (!mbar_wait_warp(&sm.dq_empty[u % kDQBufs], ((u / kDQBufs) & 1) ^ 1, g)) return -1;
+        umma_commit_warp(&sm.q_empty[u % kQBufs]);
+        umma_commit_warp(&sm.dq_full[u % kDQBufs]);
       }
     };
     // dQ of step jj of unit u (K / V load c): waits for dS, then 8 products
@@ -254,7 +291,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       const uint64_t bk = dKmn0 + st * kStageStep;
 #pragma unroll
       for (int k = 0; k < kTile / 16; ++k)  // dS from tensor memory; +2048 B of K per 16 keys
-        umma_ts_warp(tmem + kColDQ + 64 * (u & 1), tmem + kColDS + 64 * db + 8 * k, bk + 128 * k, idQ,
+        umma_ts_warp(tmem + kColDQ + kD * (u % kDQBufs), tmem + kColDS + 64 * db + 8 * k, bk + 128 * k, idQ,
                      (jj > 0 || k > 0) ? 1u : 0u);
       umma_commit_warp(&sm.ds_free[db]);
       umma_commit_warp(&sm.kv_empty[st]);
@@ -264,17 +301,17 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     uint32_t u = 0, c = 0;  // c: K / V load of the current step
     int got = fetch(n, u);
     if (got > 0) {
-      ok = issue_sdp(u & 1, c);
-      if (ok && n == 1) umma_commit_warp(&sm.q_empty[u & 1]);  // last reader of Q / dO issued
+      ok = issue_sdp(u % kQBufs, c);
+      if (ok && n == 1) umma_commit_warp(&sm.q_empty[u % kQBufs]);  // last reader of Q / dO issued
     }
     while (got > 0 && ok) {
       // the unit's first dQ waits until the read-out of the unit that used
       // this accumulator before
-      if (!mbar_wait_warp(&sm.dq_empty[u & 1], ((u >> 1) & 1) ^ 1, g)) break;
+      if (!mbar_wait_warp(&sm.dq_empty[u % kDQBufs], ((u / kDQBufs) & 1) ^ 1, g)) break;
       // every step but the last: S / dP of the next tile, then dQ of this one
       for (int jj = 0; jj + 1 < n && ok; ++jj, ++c) {
-        ok = issue_sdp(u & 1, c + 1);
-        if (ok && jj + 2 == n) umma_commit_warp(&sm.q_empty[u & 1]);
+        ok = issue_sdp(u % kQBufs, c + 1);
+        if (ok && jj + 2 == n) umma_commit_warp(&sm.q_empty[u % kQBufs]);
         if (ok) ok = dq_step(u, jj, c);
       }
       if (!ok) break;
@@ -284,11 +321,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       got = fetch(n2, u2);
       if (got < 0) break;
       if (got > 0) {
-        if (!issue_sdp(u2 & 1, c + 1)) break;
-        if (n2 == 1) umma_commit_warp(&sm.q_empty[u2 & 1]);
+        if (!issue_sdp(u2 % kQBufs, c + 1)) break;
+        if (n2 == 1) umma_commit_warp(&sm.q_empty[u2 % kQBufs]);
       }
       if (!dq_step(u, n - 1, c)) break;
-      umma_commit_warp(&sm.dq_full[u & 1]);
+      umma_commit_warp(&sm.dq_full[u % kDQBufs]);
       ++c;
       n = n2;
       u = u2;
@@ -317,26 +354,30 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       bool valid, any;
     } pend{0, 0, false, false};
     bool has_pend = false;
-    auto epilogue = [&]() -> bool {  // dq = bf16(scale * dQ), columns 32 wg .. 32 wg + 31
-      const int dqb = nunit & 1;
-      if (!mbar_wait_warp(&sm.dq_full[dqb], (nunit >> 1) & 1, g)) return false;
+    auto epilogue = [&]() -> bool {  // dq = bf16(scale * dQ), columns kD/2 wg .. kD/2 (wg + 1)
+      constexpr int kHalf = kD / 2;
+      const int dqb = nunit % kDQBufs;
+      if (!mbar_wait_warp(&sm.dq_full[dqb], (nunit / kDQBufs) & 1, g)) return false;
       ++nunit;
       tc_fence_after();
-      uint32_t a[32];
-      tmem_ld32(tmem + lane_off + kColDQ + 64 * dqb + 32 * wg, a);
+      uint32_t a[kHalf];
+      if constexpr (kHalf == 32)
+        tmem_ld32(tmem + lane_off + kColDQ + kD * dqb + kHalf * wg, a);
+      else
+        tmem_ld64(tmem + lane_off + kColDQ + kD * dqb + kHalf * wg, a);
       tc_fence_before();
       mbar_arrive(&sm.dq_empty[dqb]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sched_empty[pend.slot]);  // the slot is no longer read
       if (pend.valid) {
         const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
-        uint32_t ob[16];
+        uint32_t ob[kHalf / 2];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
+        for (int e = 0; e < kHalf / 2; ++e)
           ob[e] = pend.any ? pack_bf16(__uint_as_float(a[2 * e]) * sc, __uint_as_float(a[2 * e + 1]) * sc) : 0u;
-        uint4* dst = reinterpret_cast<uint4*>(bp.dq + pend.orow * kHeadDim + 32 * wg);
+        uint4* dst = reinterpret_cast<uint4*>(bp.dq + pend.orow * kD + kHalf * wg);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+        for (int c = 0; c < kHalf / 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
       }
       has_pend = false;
       return true;
@@ -420,8 +461,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 
 }  // namespace
 
-cudaError_t prepare_bwd_dq() {
-  return cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+cudaError_t prepare_bwd_dq(int head_dim) {
+  if (head_dim == kHeadDimWide)
+    return cudaFuncSetAttribute(dq_kernel<kHeadDimWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<kHeadDimWide>());
+  return cudaFuncSetAttribute(dq_kernel<kHeadDim>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<kHeadDim>());
 }
 
 cudaError_t launch_bwd_dq(const BwdProblem& p, const BwdLaunch& l, const TileList& qtiles,
@@ -429,7 +474,12 @@ cudaError_t launch_bwd_dq(const BwdProblem& p, const BwdLaunch& l, const TileLis
   const int64_t work = (int64_t)qtiles.capacity * p.f.Hq;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms);
   if (grid <= 0) return cudaSuccess;
-  dq_kernel<<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, l.dout, p, qtiles.items, qtiles.meta);
+  if (p.f.head_dim == kHeadDimWide)
+    dq_kernel<kHeadDimWide><<<grid, kThreads, smem_bytes<kHeadDimWide>(), s>>>(l.q, l.k, l.v, l.dout, p,
+                                                                             qtiles.items, qtiles.meta);
+  else
+    dq_kernel<kHeadDim><<<grid, kThreads, smem_bytes<kHeadDim>(), s>>>(l.q, l.k, l.v, l.dout, p,
+                                                                     qtiles.items, qtiles.meta);
   note_launch();
   return cudaGetLastError();
 }

@@ -22,8 +22,12 @@
 //   warps 2-5   softmax: one thread per query row (its TMEM lane); rescales O
 //               only when the row maximum grows by more than 2^8; writes P as
 //               bf16 into tensor memory; final O / l and LSE
-// Tensor memory (256 columns): S [0,128) fp32, P [128,192) bf16 pairs,
-// O [192,256) fp32.
+// Tensor memory at head_dim 64 (256 columns, two CTAs per SM): S [0,128)
+// fp32, P [128,192) bf16 pairs, O [192,256) fp32. At head_dim 128 (512
+// columns, one CTA per SM): S [0,128), P [128,192), O [256,384). Q, K and V
+// tiles are stored as 64-feature panels of 128-byte rows (one TMA copy and
+// one 128-byte swizzle atom width each); a product over 128 features walks
+// both panels.
 //
 // Decode instantiation (kDecode): one new query row per sequence against a
 // paged KV cache, computed exactly as the training forward computes the last
@@ -54,9 +58,17 @@ using namespace sm100;
 constexpr int kThreads = 192;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KB of bf16
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
+constexpr uint32_t kPanelBytes = kTile * 64 * 2;  // 128 rows x 64 features of bf16
+constexpr uint32_t kColS = 0, kColP = 128;
+// per head dim: tile bytes, tensor-memory columns, O's column, CTAs per SM
+template <int kD>
+struct Cfg {
+  static constexpr int kPanels = kD / 64;
+  static constexpr uint32_t kTileBytes = kPanelBytes * kPanels;
+  static constexpr uint32_t kTmemCols = kD == 64 ? 256 : 512;
+  static constexpr uint32_t kColO = kD == 64 ? 192 : 256;
+  static constexpr int kCtasPerSm = kD == 64 ? 2 : 1;
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;  // log2 units
@@ -71,11 +83,13 @@ struct Unit {
   int base, L, r0, nrows, h, kvh, kt0, kt1;
 };
 
+template <int kD>
 struct __align__(1024) Smem {
+  static constexpr uint32_t kTileBytes = Cfg<kD>::kTileBytes;
   uint8_t q[kTileBytes];
   uint8_t k[kKStages][kTileBytes];
   uint8_t v[kVStages][kTileBytes];
-  uint8_t ostage[4][32 * 128];  // per softmax warp: its 32 rows of O (bf16), 16-byte chunks swizzled
+  uint8_t ostage[4][32 * kD * 2];  // per softmax warp: its 32 rows of O (bf16), 16-byte chunks swizzled
   uint8_t zeros[kClearChunk];   // source of the bulk copies that clear the backward's dq accumulator
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
@@ -87,7 +101,10 @@ struct __align__(1024) Smem {
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+template <int kD>
+constexpr size_t smem_bytes() {
+  return sizeof(Smem<kD>) + 1024;
+}
 
 // Decode: sequence w / Hkv, kv head w % Hkv, its keys [0, L) and the 128-key
 // tiles the training forward's last row of the sequence would take.
@@ -176,13 +193,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (global_ns() - t0 > kWaitLimitNs) break;
 }
 
-template <bool kDecode>
-__global__ void __launch_bounds__(kThreads, 2)
+template <bool kDecode, int kD>
+__global__ void __launch_bounds__(kThreads, Cfg<kD>::kCtasPerSm)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, Problem p, PagedKV kv,
            const int2* __restrict__ items, int32_t* __restrict__ meta) {
+  static_assert(kD == 64 || kD == 128, "head_dim 64 or 128");
+  static_assert(!kDecode || kD == 64, "the decode instantiation is head_dim 64");
+  using C = Cfg<kD>;
+  constexpr uint32_t kTileBytes = C::kTileBytes;
+  constexpr uint32_t kTmemCols = C::kTmemCols, kColO = C::kColO;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw + align1024_pad(smem_raw));
+  Smem<kD>& sm = *reinterpret_cast<Smem<kD>*>(smem_raw + align1024_pad(smem_raw));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Guard g{&sm.abort, p.err, p.wait_limit_ns};
 
@@ -270,7 +292,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             tma_load_3d(dst + i * bs * 128, map, bar, 0, u.kvh, row);
           }
         } else {
-          tma_load_3d(dst, map, bar, 0, u.kvh, u.base + kt * kTile);
+#pragma unroll
+          for (int pi = 0; pi < C::kPanels; ++pi)
+            tma_load_3d(dst + pi * kPanelBytes, map, bar, 64 * pi, u.kvh, u.base + kt * kTile);
         }
       };
       auto load_k = [&](const Unit& u, int kt) -> bool {
@@ -303,7 +327,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           if (kDecode && u.kt1 <= u.kt0) {
             // a sequence without keys: the sink alone, o = 0 and lse = S_h
             for (int r = 0; r < u.nrows; ++r) {
-              uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)u.base * p.Hq + u.h + r) * kHeadDim);
+              uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)u.base * p.Hq + u.h + r) * kD);
               for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
               if (p.lse) p.lse[(int64_t)(u.h + r) * p.total + u.base] = p.sinks ? p.sinks[u.h + r] : -INFINITY;
             }
@@ -325,7 +349,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base);
         } else {
           mbar_expect_tx(&sm.q_full, kTileBytes);
-          tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base + u.r0);
+#pragma unroll
+          for (int pi = 0; pi < C::kPanels; ++pi)
+            tma_load_3d(sm.q + pi * kPanelBytes, &tm_q, &sm.q_full, 64 * pi, u.h, u.base + u.r0);
         }
         ++nq;
         // K runs one tile ahead of V (S(j+1) is issued before P V(j))
@@ -352,11 +378,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // The whole warp runs this loop (uniform control flow and operands); one
     // elected lane issues each product and commit.
     const uint32_t idS = idesc_bf16(kTile, kTile, false, false);
-    const uint32_t idO = idesc_bf16(kTile, kHeadDim, false, true);
-    // descriptors built once; a product adds its byte offset / 16
+    const uint32_t idO = idesc_bf16(kTile, kD, false, true);
+    // descriptors built once; a product adds its byte offset / 16. V is read
+    // MN-major: its 64-feature panels are kPanelBytes apart.
     const uint64_t dQ = sdesc_sw128(smem_u32(sm.q), 16, 1024);
     const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-    const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v[0]), 8192, 1024);
+    const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v[0]), kPanelBytes, 1024);
     constexpr uint64_t kStageStep = kTileBytes >> 4;  // k[1] - k[0], v[1] - v[0]
     uint32_t nq = 0, nk = 0, ns = 0, np = 0;
     bool ok = true;
@@ -370,8 +397,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tc_fence_after();
       const uint64_t bk = dK0 + s * kStageStep;
 #pragma unroll
-      for (int k = 0; k < kHeadDim / 16; ++k)  // +32 bytes per 16 features
-        umma_ss_warp(tmem + kColS, dQ + 2 * k, bk + 2 * k, idS, k > 0);
+      for (int k = 0; k < kD / 16; ++k) {  // +32 bytes per 16 features, panel by panel
+        const uint64_t off = (uint64_t)(k / 4) * (kPanelBytes >> 4) + 2 * (k % 4);
+        umma_ss_warp(tmem + kColS, dQ + off, bk + off, idS, k > 0);
+      }
       umma_commit_warp(&sm.s_full);
       umma_commit_warp(&sm.k_empty[s]);
       ++nk;
@@ -525,14 +554,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           ++nod;
           tc_fence_after();
           if (__any_sync(0xffffffffu, resc)) {  // O holds this unit's partial sum
-            uint32_t v[64];
-            tmem_ld64(tO, v);
-            uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-            uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st32(tO, v0);
-            tmem_st32(tO + 32, v1);
+            for (int c0 = 0; c0 < kD; c0 += 64) {
+              uint32_t v[64];
+              tmem_ld64(tO + c0, v);
+              uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+              uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+#pragma unroll
+              for (int e = 0; e < 64; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              tmem_st32(tO + c0, v0);
+              tmem_st32(tO + c0 + 32, v1);
+            }
           }
         }
         tmem_st32(tP, pa);
@@ -547,13 +579,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       ++nod;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint32_t ob[32];
-      {
+      uint32_t ob[kD / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 64) {
         uint32_t v[64];
-        tmem_ld64(tO, v);
+        tmem_ld64(tO + c0, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          ob[e] = pack_bf16(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+          ob[c0 / 2 + e] = pack_bf16(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
       }
       const int nrows = uv.nrows, row0 = uv.base + uv.r0, h = uv.h;
       __syncwarp();
@@ -561,7 +594,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if constexpr (kDecode) {  // row r: sequence base, head h + r
         const int b = row0 - uv.r0;
         if (r < nrows) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)b * p.Hq + h + r) * kHeadDim);
+          uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)b * p.Hq + h + r) * kD);
 #pragma unroll
           for (int c = 0; c < 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
           if (p.lse) p.lse[(int64_t)(h + r) * p.total + b] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
@@ -569,19 +602,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         continue;
       }
       // O rows through shared memory, so that each store instruction writes
-      // four whole 128-byte rows instead of 16 bytes of 32 rows
+      // whole rows (four of 128 bytes, or two of 256) instead of 16 bytes of
+      // 32 rows
+      constexpr int kRowBytes = kD * 2, kChunks = kD / 8, kRowsPerStore = 32 / kChunks;
       uint8_t* ost = sm.ostage[quarter];
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(ost + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+      for (int c = 0; c < kChunks; ++c)
+        *reinterpret_cast<uint4*>(ost + lane * kRowBytes + ((c ^ (lane & 7)) << 4)) =
             make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
       __syncwarp();
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int rr = 4 * k + (lane >> 3), c = lane & 7;  // row of this warp, 16-byte chunk
-        const uint4 x = *reinterpret_cast<const uint4*>(ost + rr * 128 + ((c ^ (rr & 7)) << 4));
+      for (int k = 0; k < 32 / kRowsPerStore; ++k) {
+        const int rr = kRowsPerStore * k + lane / kChunks, c = lane % kChunks;  // row of this warp, 16-byte chunk
+        const uint4 x = *reinterpret_cast<const uint4*>(ost + rr * kRowBytes + ((c ^ (rr & 7)) << 4));
         if (32 * quarter + rr < nrows)
-          reinterpret_cast<uint4*>(p.o + ((int64_t)(row0 + 32 * quarter + rr) * p.Hq + h) * kHeadDim)[c] = x;
+          reinterpret_cast<uint4*>(p.o + ((int64_t)(row0 + 32 * quarter + rr) * p.Hq + h) * kD)[c] = x;
       }
       __syncwarp();
       if (p.lse && r < nrows)
@@ -600,20 +635,30 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 }  // namespace
 
 cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l) {
-  cudaError_t e = make_tmap_bf16_rows(&l->q, p.q, p.Hq, p.total, p.q_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.k, p.Hkv, p.total, p.k_stride);
-  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.v, p.Hkv, p.total, p.v_stride);
+  const int d = p.head_dim;
+  cudaError_t e = make_tmap_bf16_rows(&l->q, p.q, p.Hq, p.total, p.q_stride, kTile, d);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.k, p.Hkv, p.total, p.k_stride, kTile, d);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.v, p.Hkv, p.total, p.v_stride, kTile, d);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (d == 128)
+    return cudaFuncSetAttribute(fwd_kernel<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<128>());
+  return cudaFuncSetAttribute(fwd_kernel<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<64>());
 }
 
 cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qtiles, int num_sms,
                        cudaStream_t s) {
   const int64_t work = (int64_t)qtiles.capacity * p.Hq;
-  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * 2);
+  const int per_sm = p.head_dim == 128 ? Cfg<128>::kCtasPerSm : Cfg<64>::kCtasPerSm;
+  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * per_sm);
   if (grid <= 0) return cudaSuccess;
-  fwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(l.q, l.k, l.v, p, PagedKV{}, qtiles.items,
-                                                       qtiles.meta);
+  if (p.head_dim == 128)
+    fwd_kernel<false, 128><<<grid, kThreads, smem_bytes<128>(), s>>>(l.q, l.k, l.v, p, PagedKV{},
+                                                                     qtiles.items, qtiles.meta);
+  else
+    fwd_kernel<false, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(l.q, l.k, l.v, p, PagedKV{},
+                                                                   qtiles.items, qtiles.meta);
   note_launch();
   return cudaGetLastError();
 }
@@ -628,13 +673,14 @@ cudaError_t launch_decode_exact(const Problem& p, const PagedKV& kv, const void*
   if (e == cudaSuccess)
     e = make_tmap_bf16_rows(&mv, v_cache, p.Hkv, rows, (int64_t)p.Hkv * kHeadDim, kv.block_size);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(fwd_kernel<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes<64>());
   if (e == cudaSuccess) e = cudaMemsetAsync(counter, 0, 2 * sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
   const int64_t work = (int64_t)p.nseq * p.Hkv;
-  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * 2);
+  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * Cfg<64>::kCtasPerSm);
   if (grid <= 0) return cudaSuccess;
-  fwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p, kv, nullptr, counter);
+  fwd_kernel<true, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(mq, mk, mv, p, kv, nullptr, counter);
   note_launch();
   return cudaGetLastError();
 }

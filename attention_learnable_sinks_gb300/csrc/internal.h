@@ -10,7 +10,8 @@
 
 namespace sinkattn {
 
-constexpr int kHeadDim = 64;
+constexpr int kHeadDim = 64;      // the head dim of decode and of the fp32 dq accumulator path
+constexpr int kHeadDimWide = 128; // the other head dim of the forward and backward
 constexpr int kTile = 128;  // rows per query tile and keys per key tile
 
 // One problem as the kernels see it. Strides are in elements per token row.
@@ -24,6 +25,7 @@ struct Problem {
   float* lse;                  // [Hq, total]
   int64_t q_stride, k_stride, v_stride;
   int32_t nseq, total, max_seqlen, Hq, Hkv, G, causal, window;
+  int32_t head_dim;            // 64 or 128
   float scale;                 // softmax scale
   float scale_log2;            // scale * log2(e)
   int32_t* err;                // device error word
@@ -45,11 +47,12 @@ struct BwdProblem {
   float* sink_part;            // [Hq, part_stride, 8] workspace: per key tile
                                // (numbered b + (cu[b] + c0) / 128) and softmax
                                // warp, sum of p_sink * P * dP
-  float* dq_acc;               // [total, Hq, 64] fp32 workspace
+  float* dq_acc;               // [total, Hq, 64] fp32 workspace (head_dim 64, atomic mode)
   int32_t nchunks;             // token chunks of the preprocess pass
   int32_t part_stride;         // key-tile capacity
   int32_t accumulate_dsinks;   // add to dsinks instead of overwriting it
-  int32_t deterministic;       // dq from the query-stationary pass (no dq_acc)
+  int32_t deterministic;       // dq from the query-stationary pass (no dq_acc);
+                               // always set at head_dim 128
   int32_t acc_cleared;         // the forward cleared dq_acc: the preprocess skips it
 };
 
@@ -113,10 +116,12 @@ __host__ __device__ inline void seeing_rows(int causal, int window, int L, int c
   *hi = h < L ? h : L;
 }
 
-// TMA descriptor for a bf16 [total, heads, 64] token-major tensor (row stride
-// in elements): 3-D {64, heads, total}, 128-byte swizzle, box {64, 1, box_rows}.
+// TMA descriptor for a bf16 [total, heads, head_dim] token-major tensor (row
+// stride in elements): 3-D {head_dim, heads, total}, 128-byte swizzle, box
+// {64, 1, box_rows}: one 64-feature panel (128-byte rows) per copy, so a
+// head_dim 128 tile takes two copies, at feature 0 and 64.
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
-                                int64_t row_stride, int box_rows = kTile);
+                                int64_t row_stride, int box_rows = kTile, int head_dim = kHeadDim);
 
 // TMA descriptor for a contiguous bf16 [rows, heads, 64] tensor read as boxes
 // of box_heads consecutive heads of one row: 3-D {64, heads, rows}, 128-byte
@@ -161,9 +166,17 @@ cudaError_t launch_bwd_finish(const BwdProblem& p, const TileList& ktiles, int n
                               cudaStream_t s);
 // Deterministic dq: query-stationary pass over the query-tile list, on the
 // main kernel's Q / K / V / dO tensor maps.
-cudaError_t prepare_bwd_dq();
+cudaError_t prepare_bwd_dq(int head_dim);
 cudaError_t launch_bwd_dq(const BwdProblem& p, const BwdLaunch& l, const TileList& qtiles,
                           int num_sms, cudaStream_t s);
+// head_dim 128: dK / dV by the key-stationary kernel over 64-row query blocks
+// (dq from the query-stationary pass). Its Q / dO maps copy 64-row boxes.
+struct BwdWideLaunch {
+  CUtensorMap q64, k, v, dout64;
+};
+cudaError_t prepare_bwd_wide(const BwdProblem& p, BwdWideLaunch* l);
+cudaError_t launch_bwd_wide(const BwdProblem& p, const BwdWideLaunch& l, const TileList& ktiles,
+                            int num_sms, cudaStream_t s);
 
 size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit);
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t s);

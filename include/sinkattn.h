@@ -25,15 +25,16 @@
  * window of W keys is the W most recent keys, the diagonal included.
  * Sequences never see each other.
  *
- * Data layout (all device memory, caller-owned):
- *   q        bf16 [total, Hq,  64], token row stride q_row_stride elements
- *   k, v     bf16 [total, Hkv, 64], token row strides k_row_stride, v_row_stride
- *   o, dout, dq   bf16 [total, Hq, 64] contiguous
- *   dk, dv        bf16 [total, Hkv, 64] contiguous
+ * Data layout (all device memory, caller-owned), d = head_dim (64 or 128;
+ * the decode entry points take 64 only):
+ *   q        bf16 [total, Hq,  d], token row stride q_row_stride elements
+ *   k, v     bf16 [total, Hkv, d], token row strides k_row_stride, v_row_stride
+ *   o, dout, dq   bf16 [total, Hq, d] contiguous
+ *   dk, dv        bf16 [total, Hkv, d] contiguous
  *   lse      fp32 [Hq, total] (head-major)
  *   sinks, dsinks  fp32 [Hq]
  *   cu_seqlens int32 [nseq + 1]: cu[0] = 0, non-decreasing, cu[nseq] = total.
- * Within a token row the heads are contiguous (head stride 64) and the 64
+ * Within a token row the heads are contiguous (head stride d) and the d
  * features are contiguous. Row strides must be multiples of 8 elements and
  * every tensor pointer must be 16-byte aligned.
  *
@@ -87,22 +88,22 @@ typedef struct sinkattn_fwd_params {
   const void* v;
   const float* sinks;          /* fp32 [Hq]; NULL = no sink (S_h = -inf)      */
   const int32_t* cu_seqlens;   /* device int32 [nseq + 1]                     */
-  void* o;                     /* out: bf16 [total, Hq, 64]                   */
+  void* o;                     /* out: bf16 [total, Hq, d]                    */
   float* lse;                  /* out: fp32 [Hq, total]; may be NULL          */
   void* workspace;             /* >= sinkattn_fwd_workspace_size() bytes       */
   size_t workspace_bytes;
   void* timing_events[2];      /* optional cudaEvent_t pair recorded on the
                                   stream just before and just after the main
                                   attention kernel; NULL entries = none      */
-  int64_t q_row_stride;        /* elements between tokens; 0 = Hq * 64        */
-  int64_t k_row_stride;        /* 0 = Hkv * 64                                */
-  int64_t v_row_stride;        /* 0 = Hkv * 64                                */
+  int64_t q_row_stride;        /* elements between tokens; 0 = Hq * d         */
+  int64_t k_row_stride;        /* 0 = Hkv * d                                 */
+  int64_t v_row_stride;        /* 0 = Hkv * d                                 */
   int32_t nseq;                /* >= 0                                        */
   int32_t total;               /* tokens = cu_seqlens[nseq] >= 0              */
   int32_t max_seqlen;          /* >= every sequence length (checked on device) */
   int32_t Hq;                  /* query heads, a multiple of Hkv              */
   int32_t Hkv;                 /* key/value heads                             */
-  int32_t head_dim;            /* must be 64 (else SINKATTN_ERR_UNSUPPORTED)  */
+  int32_t head_dim;            /* d: 64 or 128 (else SINKATTN_ERR_UNSUPPORTED) */
   int32_t causal;              /* 1 = causal mask, 0 = none                   */
   int32_t window;              /* <= 0: no window; W > 0 needs causal = 1     */
   float softmax_scale;         /* <= 0 selects 1/sqrt(head_dim)               */
@@ -116,7 +117,9 @@ typedef struct sinkattn_fwd_params {
                                   That backward, called with
                                   workspace_cleared = 1 and nothing written to
                                   the workspace in between, skips both.
-                                  Ignored by the backward.                   */
+                                  Ignored by the backward, and at head_dim
+                                  128 (whose backward has no dq accumulator
+                                  and builds its own lists).                 */
   size_t bwd_workspace_bytes;  /* >= sinkattn_bwd_workspace_size() when set    */
 } sinkattn_fwd_params;
 
@@ -126,10 +129,10 @@ typedef struct sinkattn_fwd_params {
 typedef struct sinkattn_bwd_params {
   sinkattn_fwd_params fwd;     /* fwd.o, fwd.lse are inputs here (lse required);
                                   fwd.workspace is ignored                    */
-  const void* dout;            /* bf16 [total, Hq, 64] contiguous: dL/dO       */
-  void* dq;                    /* out: bf16 [total, Hq, 64]                    */
-  void* dk;                    /* out: bf16 [total, Hkv, 64]                   */
-  void* dv;                    /* out: bf16 [total, Hkv, 64]                   */
+  const void* dout;            /* bf16 [total, Hq, d] contiguous: dL/dO        */
+  void* dq;                    /* out: bf16 [total, Hq, d]                     */
+  void* dk;                    /* out: bf16 [total, Hkv, d]                    */
+  void* dv;                    /* out: bf16 [total, Hkv, d]                    */
   float* dsinks;               /* out: fp32 [Hq]; may be NULL; the gradient is
                                   zero when sinks is NULL                     */
   void* workspace;             /* >= sinkattn_bwd_workspace_size() bytes       */
@@ -146,7 +149,10 @@ typedef struct sinkattn_bwd_params {
                                   query-stationary pass that sums the key
                                   tiles of each query tile in a fixed order,
                                   so every output is bit-identical from run to
-                                  run (dk, dv and dsinks always are).        */
+                                  run (dk, dv and dsinks always are). At
+                                  head_dim 128 the backward always takes dq
+                                  from that pass: tensor memory holds its dK
+                                  and dV accumulators with no room for dQ.  */
   void* timing_events_dq[2];   /* optional, around the deterministic dq pass
                                   (ignored when deterministic = 0)           */
   int32_t workspace_cleared;   /* nonzero: the forward of this same problem
@@ -154,13 +160,15 @@ typedef struct sinkattn_bwd_params {
                                   the dq accumulator cleared, the key-tile
                                   list built) and nothing has written to it
                                   since; the backward skips those steps.
-                                  Ignored when deterministic.                */
+                                  Ignored when deterministic and at head_dim
+                                  128.                                       */
 } sinkattn_bwd_params;
 
 /* Workspace sizes in bytes for a problem of this shape (0 on bad input).
  * sinkattn_bwd_workspace_size covers either backward mode; the deterministic
  * one needs no fp32 dq accumulator, and sinkattn_bwd_workspace_size_mode gives
- * the size for the chosen mode (deterministic != 0: the smaller one). */
+ * the size for the chosen mode (deterministic != 0: the smaller one). At
+ * head_dim 128 both give the deterministic size. */
 SINKATTN_API size_t sinkattn_fwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,
                                    int32_t head_dim);
 SINKATTN_API size_t sinkattn_bwd_workspace_size(int32_t nseq, int32_t total, int32_t Hq, int32_t Hkv,

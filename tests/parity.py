@@ -72,15 +72,15 @@ def run_cuda(w: Workload, device="cuda", q_view=None, k_view=None, v_view=None, 
     cu = w.cu_seqlens.to(device)
     do = w.dout.to(device)
     sc = w.scale if scale is None else scale
-    total, Hq, Hkv, d = w.total, w.Hq, w.Hkv, 64
+    total, Hq, Hkv, d = w.total, w.Hq, w.Hkv, w.q.shape[2]
     nseq = w.nseq
     bf, f32 = torch.bfloat16, torch.float32
     g = {"o": Guarded((total, Hq, d), bf, device), "lse": Guarded((Hq, total), f32, device),
          "dq": Guarded((total, Hq, d), bf, device), "dk": Guarded((total, Hkv, d), bf, device),
          "dv": Guarded((total, Hkv, d), bf, device), "dsinks": Guarded((Hq,), f32, device),
-         "ws_fwd": Guarded((max(api.workspace_bytes("fwd", nseq, total, Hq, Hkv), 1),),
+         "ws_fwd": Guarded((max(api.workspace_bytes("fwd", nseq, total, Hq, Hkv, head_dim=d), 1),),
                            torch.uint8, device),
-         "ws_bwd": Guarded((max(api.workspace_bytes("bwd", nseq, total, Hq, Hkv), 1),),
+         "ws_bwd": Guarded((max(api.workspace_bytes("bwd", nseq, total, Hq, Hkv, head_dim=d), 1),),
                            torch.uint8, device)}
     o, lse = api.forward(q, k, v, s, cu, max(w.max_seqlen, 1), causal=w.causal, window=w.window,
                          scale=sc, out=g["o"].t, lse=g["lse"].t, workspace=g["ws_fwd"].t)

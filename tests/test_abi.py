@@ -74,7 +74,15 @@ def test_workspace_sizes():
     b = lib.sinkattn_bwd_workspace_size(4, 8192, 64, 8, 64)
     assert 0 < f < b
     assert b >= 8192 * 64 * 64 * 4  # fp32 dq accumulator
-    assert lib.sinkattn_fwd_workspace_size(4, 8192, 64, 8, 128) == 0
+    assert lib.sinkattn_fwd_workspace_size(4, 8192, 64, 8, 96) == 0
+    assert lib.sinkattn_bwd_workspace_size(4, 8192, 64, 8, 256) == 0
+    # head_dim 128: same lists; the backward is always the deterministic one
+    # (no fp32 dq accumulator), whatever mode is asked for
+    assert lib.sinkattn_fwd_workspace_size(4, 8192, 64, 8, 128) == f
+    det = lib.sinkattn_bwd_workspace_size_mode(4, 8192, 64, 8, 64, 1)
+    assert det < b
+    assert lib.sinkattn_bwd_workspace_size(4, 8192, 64, 8, 128) == det
+    assert lib.sinkattn_bwd_workspace_size_mode(4, 8192, 64, 8, 128, 0) == det
     assert lib.sinkattn_bwd_workspace_size(4, 8192, 63, 8, 64) == 0
     assert lib.sinkattn_bwd_workspace_size(-1, 8192, 64, 8, 64) == 0
 
@@ -100,7 +108,9 @@ def _params(**kw):
 
 
 @pytest.mark.parametrize("change,status", [
-    ({"head_dim": 128}, 2),
+    ({"head_dim": 96}, 2),
+    ({"head_dim": 256}, 2),
+    ({"head_dim": 128, "q_row_stride": 4 * 64}, 1),  # covers the heads at 64, not at 128
     ({"Hq": 5}, 1),
     ({"Hkv": 0}, 1),
     ({"causal": 0, "window": 16}, 2),
