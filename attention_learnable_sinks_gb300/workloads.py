@@ -25,6 +25,8 @@ rounded to bf16 with round-to-nearest-even):
   long         seed 5  B=1  T=32768 Hq=64 Hkv=8 causal            q,k ~ 2 N(0,1)      S ~ U(-10,10)
                                                                   v,dO ~ N(0,1)
   long_window  seed 5  as long, causal window of 128 keys
+  dense_d128   seed 12 as dense at head_dim 128 (the head width of the
+                       training log on page 4, the xxqk.cn post)           N(0,1)     S ~ U(-2,2)
 """
 
 from __future__ import annotations
@@ -118,6 +120,7 @@ CONFIGS = {
     "long": dict(lengths=[32768], Hq=64, Hkv=8, seed=5, qk_std=2.0, sink_range=(-10.0, 10.0)),
     "long_window": dict(lengths=[32768], Hq=64, Hkv=8, seed=5, qk_std=2.0,
                         sink_range=(-10.0, 10.0), window=128),
+    "dense_d128": dict(lengths=[2048] * 4, Hq=64, Hkv=8, seed=12, d=128),
 }
 
 # One-line descriptions, used in reports.
@@ -128,6 +131,7 @@ DESCRIPTIONS = {
     "varlen": "32 packed seqs L~U[256,8192] Hq=64 Hkv=8 d=64 causal, odd-head sinks -30",
     "long": "B=1 T=32768 Hq=64 Hkv=8 d=64 causal, q,k~2N(0,1), S~U(-10,10)",
     "long_window": "B=1 T=32768 Hq=64 Hkv=8 d=64 causal window=128, q,k~2N(0,1)",
+    "dense_d128": "B=4 T=2048 Hq=64 Hkv=8 d=128 causal",
 }
 
 

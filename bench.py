@@ -72,9 +72,9 @@ def allowed_pairs(lengths, causal: bool, window: int) -> int:
     return n
 
 
-def step_flops(lengths, Hq, causal, window):
+def step_flops(lengths, Hq, causal, window, d=HEAD_DIM):
     pairs = allowed_pairs(lengths, causal, window)
-    return 4 * HEAD_DIM * pairs * Hq, 10 * HEAD_DIM * pairs * Hq
+    return 4 * d * pairs * Hq, 10 * d * pairs * Hq
 
 
 def load_peaks():
@@ -287,7 +287,7 @@ def run_reference(args):
 def workload_config(w, name):
     from attention_learnable_sinks_gb300.workloads import DESCRIPTIONS
     return {"workload": f"{name}: {DESCRIPTIONS[name]}", "nseq": w.nseq, "total_tokens": w.total,
-            "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": HEAD_DIM, "causal": w.causal,
+            "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": int(w.q.shape[2]), "causal": w.causal,
             "window": w.window, "l2": L2_NOTE,
             "flop_convention": "14*d*N_allowed_pairs*Hq (fwd 4*d, bwd 10*d)"}
 
@@ -305,23 +305,24 @@ def run_gb300(args):
     _binding.lib()
     w = workloads.config(args.workload)
     lengths = w.meta["lengths"]
-    fwd_flops, bwd_flops = step_flops(lengths, w.Hq, w.causal, w.window)
+    hd = int(w.q.shape[2])
+    fwd_flops, bwd_flops = step_flops(lengths, w.Hq, w.causal, w.window, hd)
     flops = fwd_flops + bwd_flops
 
     q, k, v, do = (t.to(device) for t in (w.q, w.k, w.v, w.dout))
     s, cu = w.sinks.to(device), w.cu_seqlens.to(device)
     maxlen = w.max_seqlen
     total, Hq, Hkv = w.total, w.Hq, w.Hkv
-    o = torch.empty(total, Hq, HEAD_DIM, dtype=torch.bfloat16, device=device)
+    o = torch.empty(total, Hq, hd, dtype=torch.bfloat16, device=device)
     lse = torch.empty(Hq, total, dtype=torch.float32, device=device)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     ds = torch.empty(Hq, dtype=torch.float32, device=device)
-    ws_f = torch.empty(api.workspace_bytes("fwd", w.nseq, total, Hq, Hkv), dtype=torch.uint8,
-                       device=device)
-    ws_b = torch.empty(api.workspace_bytes("bwd", w.nseq, total, Hq, Hkv), dtype=torch.uint8,
-                       device=device)
+    ws_f = torch.empty(api.workspace_bytes("fwd", w.nseq, total, Hq, Hkv, head_dim=hd),
+                       dtype=torch.uint8, device=device)
+    ws_b = torch.empty(api.workspace_bytes("bwd", w.nseq, total, Hq, Hkv, head_dim=hd),
+                       dtype=torch.uint8, device=device)
     flush = L2Flush(device)
 
     def new_events(n):
@@ -331,7 +332,8 @@ def run_gb300(args):
         return evs
 
     K = args.steps
-    det = args.deterministic
+    # head_dim 128 always takes dq from the fixed-order query-stationary pass
+    det = args.deterministic or hd != HEAD_DIM
     step_ev = [new_events(2) for _ in range(K)]
     fwd_ev = [new_events(2) for _ in range(K)]
     bwd_ev = [new_events(2) for _ in range(K)]
@@ -395,7 +397,7 @@ def run_gb300(args):
     hds = torch.empty(ds.shape, dtype=ds.dtype).pin_memory()
     pipe = api.HostPipeline(w.cu_seqlens, w.Hq, w.Hkv, causal=w.causal, window=w.window,
                             scale=w.scale, groups=args.e2e_groups, device=device,
-                            deterministic=det)
+                            deterministic=det, head_dim=hd)
     h2d, d2h = pipe.h2d_bytes(), pipe.d2h_bytes()
 
     def e2e_step():
@@ -427,7 +429,8 @@ def run_gb300(args):
     # algorithmic work is its dk / dv products (S, dP, dV, dK: 4 of 5)
     dq_flops = 1.5 * fwd_flops
     main_flops = 0.8 * bwd_flops if det else bwd_flops
-    cands = [("fwd", f_avg, fwd_flops, "fwd.cu"), ("bwd main", b_avg, main_flops, "bwd.cu")]
+    cands = [("fwd", f_avg, fwd_flops, "fwd.cu"),
+             ("bwd main", b_avg, main_flops, "bwd.cu" if hd == HEAD_DIM else "bwd_wide.cu")]
     if det:
         cands.append(("dq pass", q_avg, dq_flops, "dq.cu"))
     dom, dom_ms, dom_flops, dom_file = max(cands, key=lambda c: c[1])
@@ -442,7 +445,7 @@ def run_gb300(args):
         #   backward main: read q, dO, k, v, LSE, D; write dk, dv and the fp32
         #                  dq accumulator once (no accumulator when deterministic)
         #   dq pass:       read q, dO, k, v, LSE, D; write dq
-        d, Hq, Hkv = 64, w.Hq, w.Hkv
+        d, Hq, Hkv = hd, w.Hq, w.Hkv
         per_tok = {"fwd": 2 * Hq * d + 4 * Hkv * d + 2 * Hq * d + 4 * Hq,
                    "bwd main": 4 * Hq * d + 4 * Hkv * d + 8 * Hq + 4 * Hkv * d + (0 if det else 4 * Hq * d),
                    "dq pass": 4 * Hq * d + 4 * Hkv * d + 8 * Hq + 2 * Hq * d}[dom]
@@ -697,7 +700,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", default="dense",
                     choices=("tiny", "dense", "window", "varlen", "long", "long_window",
-                             "decode", "decode_window"))
+                             "dense_d128", "decode", "decode_window"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
                     help="backward with dq summed in a fixed order (query-stationary dq pass)")
