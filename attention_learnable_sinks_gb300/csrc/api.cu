@@ -275,7 +275,7 @@ cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int tota
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)total};
   const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 4, (cuuint64_t)heads * kHeadDim * 4};
-  const cuuint32_t box[3] = {32, 1, (cuuint32_t)kTile};
+  const cuuint32_t box[3] = {32, 1, 32};  // 32 rows: one read-out warp's share of a tile
   const cuuint32_t elem[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, elem,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -130,7 +130,7 @@ cudaError_t make_tmap_bf16_heads(CUtensorMap* map, const void* base, int heads, 
                                  int box_heads);
 
 // TMA descriptor for the fp32 [total, heads, 64] dq accumulator (contiguous):
-// 3-D {64, heads, total}, 128-byte swizzle, box {32, 1, 128}.
+// 3-D {64, heads, total}, 128-byte swizzle, box {32, 1, 32}.
 cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int total);
 
 // Launchers (each returns the cudaGetLastError() of its launch).
