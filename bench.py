@@ -435,8 +435,9 @@ def run_gb300(args):
         cands.append(("dq pass", q_avg, dq_flops, "dq.cu"))
     dom, dom_ms, dom_flops, dom_file = max(cands, key=lambda c: c[1])
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
-    dom_key = dom_file + ("#deterministic" if det and dom == "bwd main" else "")
-    tr = traffic_record(dom_key) if args.workload == "dense" else None
+    dom_key = dom_file + ("#deterministic" if det and dom_file == "bwd.cu" else "")
+    # counters were taken on the dense workloads; other workloads have none
+    tr = traffic_record(dom_key if args.workload == "dense" else f"{dom_key}@{args.workload}")
     if w.window > 0:
         # a band of W keys: about W flop per byte moved, below the ridge
         # (1910.8 TFLOP/s / 6786.6 GB/s = 282 flop/B), so HBM bounds it.
