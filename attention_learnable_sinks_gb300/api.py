@@ -153,19 +153,21 @@ def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, s
            num_splits=0, out=None, lse=None, workspace=None, exact=False):
     """One query row per sequence against a paged KV cache.
 
-    q [nseq, Hq, 64] bf16; k_cache, v_cache [num_blocks, block_size, Hkv, 64]
+    q [nseq, Hq, d] bf16; k_cache, v_cache [num_blocks, block_size, Hkv, d]
     bf16; block_table [nseq, max_blocks] int32; seqlens [nseq] int32 (keys per
-    sequence, the new token's included). Returns o [nseq, Hq, 64] bf16 and
+    sequence, the new token's included). Returns o [nseq, Hq, d] bf16 and
     lse [Hq, nseq] fp32: the last row of ``forward`` over each sequence. With
     ``exact`` each row is computed exactly as ``forward`` computes that last
-    row, so the two agree bit for bit (num_splits is then ignored)."""
+    row, so the two agree bit for bit (num_splits is then ignored). d is 64,
+    or 128 with ``exact``."""
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
-    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
-        raise ValueError("q must be [nseq, Hq, 64]")
-    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.shape[3] != HEAD_DIM:
-        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, Hkv, 64]")
+    dims = HEAD_DIMS if exact else (HEAD_DIM,)
+    if q.dim() != 3 or q.shape[2] not in dims:
+        raise ValueError(f"q must be [nseq, Hq, d] with d in {dims}")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.shape[3] != q.shape[2]:
+        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, Hkv, d]")
     for name, t in (("block_table", block_table), ("seqlens", seqlens)):
         if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")

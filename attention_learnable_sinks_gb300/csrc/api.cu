@@ -256,12 +256,12 @@ cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, i
 }
 
 cudaError_t make_tmap_bf16_heads(CUtensorMap* map, const void* base, int heads, int rows,
-                                 int box_heads) {
+                                 int box_heads, int head_dim) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)box_heads, 1};
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_heads, 1};
   const cuuint32_t elem[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -446,10 +446,12 @@ namespace {
 
 // Checks shared by both decode entry points (nothing to do: nseq == 0 gives
 // SINKATTN_OK with *empty set).
-sinkattn_status check_decode(const sinkattn_decode_params* a, bool* empty) {
+sinkattn_status check_decode(const sinkattn_decode_params* a, bool* empty, bool exact) {
   *empty = false;
   if (!a) return fail(SINKATTN_ERR_INVALID_ARG, "params is NULL");
-  if (a->head_dim != kHeadDim) return fail(SINKATTN_ERR_UNSUPPORTED, "head_dim must be 64");
+  if (exact ? !head_dim_ok(a->head_dim) : a->head_dim != kHeadDim)
+    return fail(SINKATTN_ERR_UNSUPPORTED,
+                exact ? "head_dim must be 64 or 128" : "head_dim must be 64 (128: sinkattn_decode_exact)");
   if (a->nseq < 0 || a->nseq > 65535 || a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv || a->Hq > 65535)
     return fail(SINKATTN_ERR_INVALID_ARG, "need 0 <= nseq <= 65535, 0 < Hkv, Hq % Hkv == 0, Hq <= 65535");
   const int G = a->Hq / a->Hkv;
@@ -483,7 +485,7 @@ extern "C" {
 sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
   g_message.clear();
   bool empty = false;
-  sinkattn_status st0 = check_decode(a, &empty);
+  sinkattn_status st0 = check_decode(a, &empty, false);
   if (st0 != SINKATTN_OK || empty) return st0;
   if (!a->workspace ||
       a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, std::max(a->num_splits, 1)))
@@ -552,7 +554,7 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
 sinkattn_status sinkattn_decode_exact(const sinkattn_decode_params* a, void* stream) {
   g_message.clear();
   bool empty = false;
-  sinkattn_status st = check_decode(a, &empty);
+  sinkattn_status st = check_decode(a, &empty, true);
   if (st != SINKATTN_OK || empty) return st;
   if (!a->workspace || a->workspace_bytes < 256)
     return fail(SINKATTN_ERR_WORKSPACE, "the exact decode needs a workspace of at least 256 bytes");
@@ -570,8 +572,9 @@ sinkattn_status sinkattn_decode_exact(const sinkattn_decode_params* a, void* str
   p.Hkv = a->Hkv;
   p.G = a->Hq / a->Hkv;
   p.causal = 1;
+  p.head_dim = a->head_dim;
   p.window = a->window > 0 ? a->window : 0;
-  p.scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+  p.scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)a->head_dim);
   p.scale_log2 = p.scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.withhold_copies = withhold_copies();

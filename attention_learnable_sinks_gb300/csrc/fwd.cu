@@ -199,7 +199,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
            const __grid_constant__ CUtensorMap tm_v, Problem p, PagedKV kv,
            const int2* __restrict__ items, int32_t* __restrict__ meta) {
   static_assert(kD == 64 || kD == 128, "head_dim 64 or 128");
-  static_assert(!kDecode || kD == 64, "the decode instantiation is head_dim 64");
   using C = Cfg<kD>;
   constexpr uint32_t kTileBytes = C::kTileBytes;
   constexpr uint32_t kTmemCols = C::kTmemCols, kColO = C::kColO;
@@ -289,7 +288,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
               else
                 atomicCAS(p.err, 0, 1 /* SINKATTN_ERR_INVALID_ARG */);
             }
-            tma_load_3d(dst + i * bs * 128, map, bar, 0, u.kvh, row);
+#pragma unroll
+            for (int pi = 0; pi < C::kPanels; ++pi)
+              tma_load_3d(dst + pi * kPanelBytes + i * bs * 128, map, bar, 64 * pi, u.kvh, row);
           }
         } else {
 #pragma unroll
@@ -328,7 +329,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             // a sequence without keys: the sink alone, o = 0 and lse = S_h
             for (int r = 0; r < u.nrows; ++r) {
               uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)u.base * p.Hq + u.h + r) * kD);
-              for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+              for (int c = 0; c < kD / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
               if (p.lse) p.lse[(int64_t)(u.h + r) * p.total + u.base] = p.sinks ? p.sinks[u.h + r] : -INFINITY;
             }
             continue;
@@ -345,8 +346,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (p.withhold_copies) break;  // test hook: the consumers' waits run out
         if (!mbar_wait(&sm.q_empty, (nq & 1) ^ 1, g)) break;
         if (kDecode) {  // the G heads' rows of this sequence into rows 0 .. G-1
-          mbar_expect_tx(&sm.q_full, (uint32_t)u.nrows * 128u);
-          tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, u.h, u.base);
+          mbar_expect_tx(&sm.q_full, (uint32_t)u.nrows * 128u * C::kPanels);
+#pragma unroll
+          for (int pi = 0; pi < C::kPanels; ++pi)
+            tma_load_3d(sm.q + pi * kPanelBytes, &tm_q, &sm.q_full, 64 * pi, u.h, u.base);
         } else {
           mbar_expect_tx(&sm.q_full, kTileBytes);
 #pragma unroll
@@ -437,8 +440,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           // written) are zeroed, as the training forward's are finite there
           const int rs = u.L - (u.kt0 + jj) * kTile;
           if (rs < kTile) {
-            for (int e = lane; e < (kTile - rs) * 8; e += 32)
-              *reinterpret_cast<uint4*>(sm.v[sv] + (rs + e / 8) * 128 + (e % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            for (int e = lane; e < (kTile - rs) * 8 * C::kPanels; e += 32) {
+              const int pi = e / ((kTile - rs) * 8), f = e % ((kTile - rs) * 8);
+              *reinterpret_cast<uint4*>(sm.v[sv] + pi * kPanelBytes + (rs + f / 8) * 128 + (f % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
             fence_async_smem();
             __syncwarp();
           }
@@ -596,7 +602,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (r < nrows) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + ((int64_t)b * p.Hq + h + r) * kD);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+          for (int c = 0; c < kD / 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
           if (p.lse) p.lse[(int64_t)(h + r) * p.total + b] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         }
         continue;
@@ -667,20 +673,27 @@ cudaError_t launch_decode_exact(const Problem& p, const PagedKV& kv, const void*
                                 const void* v_cache, int32_t* counter, int num_sms, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   const int rows = kv.num_blocks * kv.block_size;
-  cudaError_t e = make_tmap_bf16_heads(&mq, p.q, p.Hq, p.nseq, p.G);
+  const int d = p.head_dim;
+  cudaError_t e = make_tmap_bf16_heads(&mq, p.q, p.Hq, p.nseq, p.G, d);
   if (e == cudaSuccess)
-    e = make_tmap_bf16_rows(&mk, k_cache, p.Hkv, rows, (int64_t)p.Hkv * kHeadDim, kv.block_size);
+    e = make_tmap_bf16_rows(&mk, k_cache, p.Hkv, rows, (int64_t)p.Hkv * d, kv.block_size, d);
   if (e == cudaSuccess)
-    e = make_tmap_bf16_rows(&mv, v_cache, p.Hkv, rows, (int64_t)p.Hkv * kHeadDim, kv.block_size);
+    e = make_tmap_bf16_rows(&mv, v_cache, p.Hkv, rows, (int64_t)p.Hkv * d, kv.block_size, d);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fwd_kernel<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes<64>());
+    e = d == 128 ? cudaFuncSetAttribute(fwd_kernel<true, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem_bytes<128>())
+                 : cudaFuncSetAttribute(fwd_kernel<true, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem_bytes<64>());
   if (e == cudaSuccess) e = cudaMemsetAsync(counter, 0, 2 * sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
   const int64_t work = (int64_t)p.nseq * p.Hkv;
-  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * Cfg<64>::kCtasPerSm);
+  const int per_sm = d == 128 ? Cfg<128>::kCtasPerSm : Cfg<64>::kCtasPerSm;
+  const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * per_sm);
   if (grid <= 0) return cudaSuccess;
-  fwd_kernel<true, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(mq, mk, mv, p, kv, nullptr, counter);
+  if (d == 128)
+    fwd_kernel<true, 128><<<grid, kThreads, smem_bytes<128>(), s>>>(mq, mk, mv, p, kv, nullptr, counter);
+  else
+    fwd_kernel<true, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(mq, mk, mv, p, kv, nullptr, counter);
   note_launch();
   return cudaGetLastError();
 }

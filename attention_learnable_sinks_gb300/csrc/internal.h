@@ -123,11 +123,11 @@ __host__ __device__ inline void seeing_rows(int causal, int window, int L, int c
 cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, int total,
                                 int64_t row_stride, int box_rows = kTile, int head_dim = kHeadDim);
 
-// TMA descriptor for a contiguous bf16 [rows, heads, 64] tensor read as boxes
-// of box_heads consecutive heads of one row: 3-D {64, heads, rows}, 128-byte
-// swizzle, box {64, box_heads, 1}.
+// TMA descriptor for a contiguous bf16 [rows, heads, head_dim] tensor read as
+// boxes of 64 features of box_heads consecutive heads of one row: 3-D
+// {head_dim, heads, rows}, 128-byte swizzle, box {64, box_heads, 1}.
 cudaError_t make_tmap_bf16_heads(CUtensorMap* map, const void* base, int heads, int rows,
-                                 int box_heads);
+                                 int box_heads, int head_dim = kHeadDim);
 
 // TMA descriptor for the fp32 [total, heads, 64] dq accumulator (contiguous):
 // 3-D {64, heads, total}, 128-byte swizzle, box {32, 1, 32}.
@@ -154,7 +154,7 @@ cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l);
 cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l);
 cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qtiles, int num_sms,
                        cudaStream_t s);
-// Exact decode: p describes nseq query rows [nseq, Hq, 64] (q, o, lse [Hq, nseq],
+// Exact decode: p describes nseq query rows [nseq, Hq, head_dim] (q, o, lse [Hq, nseq],
 // sinks, window, scale); the keys come from kv. counter: one int of device
 // memory, zeroed here before the launch (work stealing).
 cudaError_t launch_decode_exact(const Problem& p, const PagedKV& kv, const void* k_cache,

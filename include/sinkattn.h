@@ -26,7 +26,7 @@
  * Sequences never see each other.
  *
  * Data layout (all device memory, caller-owned), d = head_dim (64 or 128;
- * the decode entry points take 64 only):
+ * sinkattn_decode takes 64 only):
  *   q        bf16 [total, Hq,  d], token row stride q_row_stride elements
  *   k, v     bf16 [total, Hkv, d], token row strides k_row_stride, v_row_stride
  *   o, dout, dq   bf16 [total, Hq, d] contiguous
@@ -216,15 +216,15 @@ SINKATTN_API sinkattn_status sinkattn_bwd_static_workspace(const sinkattn_bwd_pa
  * The keys are split into up to num_splits ranges processed side by side;
  * the partial results are merged with the sink in a second kernel.
  *
- * Layouts:
- *   q            bf16 [nseq, Hq, 64] contiguous
- *   k_cache,     bf16 [num_blocks, block_size, Hkv, 64] contiguous; logical
+ * Layouts (d = head_dim: 64; sinkattn_decode_exact also takes 128):
+ *   q            bf16 [nseq, Hq, d] contiguous
+ *   k_cache,     bf16 [num_blocks, block_size, Hkv, d] contiguous; logical
  *   v_cache      block i of sequence b is physical block block_table[b][i]
  *   block_table  int32 [nseq, max_blocks_per_seq]; entries for blocks past a
  *                sequence's last key or wholly before its window are ignored,
  *                the others must be in [0, num_blocks)
  *   seqlens      int32 [nseq], 0 <= seqlens[b] <= max_blocks_per_seq * block_size
- *   o            bf16 [nseq, Hq, 64] (out)
+ *   o            bf16 [nseq, Hq, d] (out)
  *   lse          fp32 [Hq, nseq] natural log (out; may be NULL)
  * block_size must be 16, 32, 64 or 128; Hq / Hkv must be 1, 2, 4, 8 or 16.
  * A sequence with no keys gets o = 0 and lse = S_h (the sink alone). Device
@@ -248,7 +248,7 @@ typedef struct sinkattn_decode_params {
   int32_t max_blocks_per_seq;  /* columns of block_table                       */
   int32_t Hq;
   int32_t Hkv;
-  int32_t head_dim;            /* must be 64                                   */
+  int32_t head_dim;            /* 64 (sinkattn_decode_exact: 64 or 128)       */
   int32_t window;              /* <= 0: every key; W > 0: the last W keys      */
   int32_t num_splits;          /* key ranges per sequence, 1..64; 0 = choose    */
   float softmax_scale;         /* <= 0 selects 1/sqrt(head_dim)                */
@@ -276,7 +276,9 @@ SINKATTN_API sinkattn_status sinkattn_decode(const sinkattn_decode_params* param
  * longer than with sinkattn_decode. workspace: at least 256 bytes (a work
  * counter, cleared by the call). Cache slots past a sequence's last key and
  * blocks wholly before its window are not read. Block indices out of range
- * set SINKATTN_ERR_INVALID_ARG in the device error word and read as zeros. */
+ * set SINKATTN_ERR_INVALID_ARG in the device error word and read as zeros.
+ * head_dim may be 128 here (the training forward's head_dim 128 kernel, in
+ * its decode form). */
 SINKATTN_API sinkattn_status sinkattn_decode_exact(const sinkattn_decode_params* params, void* stream);
 
 /* Static description of a status code; never NULL. */

@@ -212,6 +212,23 @@ def test_decode_rejects_bad_arguments(change, status):
     assert lib.sinkattn_launch_count() == n0
 
 
+@pytest.mark.parametrize("change,status", [
+    ({"head_dim": 96}, 2),
+    ({"head_dim": 256}, 2),
+    ({"head_dim": 128, "block_size": 8}, 2),   # head_dim 128 passes; the block size does not
+    ({"head_dim": 128, "q": None}, 1),
+    ({"workspace_bytes": 8}, 4),
+])
+def test_exact_decode_rejects_bad_arguments(change, status):
+    # the exact decode takes head_dim 64 or 128; every case fails before a launch
+    lib = _binding.lib()
+    n0 = lib.sinkattn_launch_count()
+    p, buf = _decode_params(**change)
+    assert lib.sinkattn_decode_exact(ctypes.byref(p), None) == status
+    assert lib.sinkattn_last_error_message()
+    assert lib.sinkattn_launch_count() == n0
+
+
 def test_decode_without_sequences_needs_no_device():
     lib = _binding.lib()
     p, buf = _decode_params(nseq=0, q=None, workspace=None)

@@ -38,8 +38,11 @@ def _expect_timeout(fn):
     assert _binding.device_error(reset=True) == TIMEOUT
 
 
-def test_forward_and_backward_waits_run_out_then_recover(cuda_lib):
-    w = make("watchdog", [300, 129, 640], 8, 2, seed=31)
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_and_backward_waits_run_out_then_recover(cuda_lib, d):
+    # head_dim 128: the 128-feature forward, the dK / dV block kernel and the
+    # 128-feature dq pass
+    w = make(f"watchdog_d{d}", [300, 129, 640], 8, 2, seed=31, d=d)
     dev = "cuda"
     q, k, v, do = (t.to(dev) for t in (w.q, w.k, w.v, w.dout))
     s, cu = w.sinks.to(dev), w.cu_seqlens.to(dev)

@@ -88,6 +88,22 @@ def test_static_workspace_deterministic_fits_larger_problems(cuda_lib):
     _check(prob.static(True), prob.regular(True))
 
 
+def test_static_workspace_head_dim128_in_either_mode(cuda_lib):
+    # head_dim 128 always takes the deterministic backward, so the dense
+    # shape fits whichever mode is asked for, and both give the same bits
+    w = make("noalloc_d128", [2048] * 4, 64, 8, seed=24, d=128)
+    need = api.workspace_bytes("bwd", w.nseq, w.total, w.Hq, w.Hkv, head_dim=128)
+    assert need == api.workspace_bytes("bwd", w.nseq, w.total, w.Hq, w.Hkv, deterministic=True,
+                                       head_dim=128)
+    assert need <= STATIC_BYTES
+    prob = _Problem(w)
+    ref = prob.regular(False)
+    for det in (False, True):
+        got = prob.static(det)
+        for g, r in zip(got, ref):
+            assert torch.equal(g, r)
+
+
 def test_static_workspace_rejects_problems_above_its_size(cuda_lib):
     lib = _binding.lib()
     p = BwdParams()
