@@ -64,3 +64,24 @@ def test_long_full_group(cuda_lib):
         errs = compare_full(w, got, ref, tok, qh, kvh)
         errs["dsinks"] = assert_dsinks(got["dsinks"][qh], ref["dsinks"], cond)
         print("long", "deterministic" if det else "atomic", {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+def test_many_short_sequences(cuda_lib):
+    """6000 ragged sequences of 1-40 tokens (Hq=16, Hkv=2): the fp32 dq
+    accumulator (~0.5 GB) is far beyond L2, so the atomic backward hands out key
+    tiles sequence by sequence, and with more sequences than its 4096-entry
+    bucket table separates, the later sequences share the last bucket. One
+    complete GQA group over every sequence, element by element, both modes."""
+    import torch
+    from attention_learnable_sinks_gb300.workloads import make
+    g = torch.Generator().manual_seed(61)
+    lens = torch.randint(1, 41, (6000,), generator=g).tolist()
+    w = make("many_short", lens, 16, 2, seed=62)
+    assert w.total * w.Hq * 64 * 4 > (192 << 20) and w.nseq > 4096
+    ref, tok, qh, kvh = run_oracle(w, kv_groups=[1])
+    cond = dsink_condition(w.sinks.numpy().astype(np.float64)[qh], ref["lse"], ref["o"],
+                           ref["_do"])
+    for det in (False, True):
+        got = run_cuda(w, deterministic=det)
+        errs = compare_full(w, got, ref, tok, qh, kvh)
+        errs["dsinks"] = assert_dsinks(got["dsinks"][qh], ref["dsinks"], cond)
