@@ -77,6 +77,8 @@ SYMBOLS = [
     ("sinkattn_last_error_message", ctypes.c_char_p, []),
     ("sinkattn_device_error", ctypes.c_int32, [ctypes.c_int32]),
     ("sinkattn_launch_count", ctypes.c_uint64, []),
+    ("sinkattn_decode_workspace_size_d", ctypes.c_size_t,
+     [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("sinkattn_params_size", ctypes.c_size_t, [ctypes.c_int32]),
     ("sinkattn_set_wait_limit_ns", None, [ctypes.c_uint64]),
     ("sinkattn_test_withhold_copies", None, [ctypes.c_int32]),

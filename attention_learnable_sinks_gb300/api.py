@@ -158,14 +158,13 @@ def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, s
     sequence, the new token's included). Returns o [nseq, Hq, d] bf16 and
     lse [Hq, nseq] fp32: the last row of ``forward`` over each sequence. With
     ``exact`` each row is computed exactly as ``forward`` computes that last
-    row, so the two agree bit for bit (num_splits is then ignored). d is 64,
-    or 128 with ``exact``."""
+    row, so the two agree bit for bit (num_splits is then ignored). d is 64
+    or 128."""
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
-    dims = HEAD_DIMS if exact else (HEAD_DIM,)
-    if q.dim() != 3 or q.shape[2] not in dims:
-        raise ValueError(f"q must be [nseq, Hq, d] with d in {dims}")
+    if q.dim() != 3 or q.shape[2] not in HEAD_DIMS:
+        raise ValueError(f"q must be [nseq, Hq, d] with d in {HEAD_DIMS}")
     if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.shape[3] != q.shape[2]:
         raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, Hkv, d]")
     for name, t in (("block_table", block_table), ("seqlens", seqlens)):
@@ -181,8 +180,8 @@ def decode(q, k_cache, v_cache, block_table, seqlens, sinks=None, *, window=0, s
     o = out if out is not None else torch.empty(nseq, Hq, d, dtype=torch.bfloat16, device=q.device)
     lse = lse if lse is not None else torch.empty(Hq, nseq, dtype=torch.float32, device=q.device)
     if workspace is None:
-        nbytes = 256 if exact else L.sinkattn_decode_workspace_size(
-            nseq, Hq, num_splits if num_splits > 0 else 64)
+        nbytes = 256 if exact else L.sinkattn_decode_workspace_size_d(
+            nseq, Hq, num_splits if num_splits > 0 else 64, d)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     p = DecodeParams()
     p.q, p.k_cache, p.v_cache = _ptr(q), _ptr(k_cache), _ptr(v_cache)

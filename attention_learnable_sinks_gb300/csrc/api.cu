@@ -436,8 +436,13 @@ sinkattn_status sinkattn_bwd(const sinkattn_bwd_params* a, void* stream) {
 }
 
 size_t sinkattn_decode_workspace_size(int32_t nseq, int32_t Hq, int32_t num_splits) {
-  if (nseq < 0 || Hq <= 0 || Hq > 65535 || num_splits < 1 || num_splits > 64) return 0;
-  return decode_workspace_bytes(nseq, Hq, num_splits);
+  return sinkattn_decode_workspace_size_d(nseq, Hq, num_splits, kHeadDim);
+}
+
+size_t sinkattn_decode_workspace_size_d(int32_t nseq, int32_t Hq, int32_t num_splits, int32_t head_dim) {
+  if (nseq < 0 || Hq <= 0 || Hq > 65535 || num_splits < 1 || num_splits > 64 || !head_dim_ok(head_dim))
+    return 0;
+  return decode_workspace_bytes(nseq, Hq, num_splits, head_dim);
 }
 
 }  // extern "C"
@@ -446,12 +451,10 @@ namespace {
 
 // Checks shared by both decode entry points (nothing to do: nseq == 0 gives
 // SINKATTN_OK with *empty set).
-sinkattn_status check_decode(const sinkattn_decode_params* a, bool* empty, bool exact) {
+sinkattn_status check_decode(const sinkattn_decode_params* a, bool* empty) {
   *empty = false;
   if (!a) return fail(SINKATTN_ERR_INVALID_ARG, "params is NULL");
-  if (exact ? !head_dim_ok(a->head_dim) : a->head_dim != kHeadDim)
-    return fail(SINKATTN_ERR_UNSUPPORTED,
-                exact ? "head_dim must be 64 or 128" : "head_dim must be 64 (128: sinkattn_decode_exact)");
+  if (!head_dim_ok(a->head_dim)) return fail(SINKATTN_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (a->nseq < 0 || a->nseq > 65535 || a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv || a->Hq > 65535)
     return fail(SINKATTN_ERR_INVALID_ARG, "need 0 <= nseq <= 65535, 0 < Hkv, Hq % Hkv == 0, Hq <= 65535");
   const int G = a->Hq / a->Hkv;
@@ -485,11 +488,12 @@ extern "C" {
 sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
   g_message.clear();
   bool empty = false;
-  sinkattn_status st0 = check_decode(a, &empty, false);
+  sinkattn_status st0 = check_decode(a, &empty);
   if (st0 != SINKATTN_OK || empty) return st0;
+  const int32_t d = a->head_dim;
   if (!a->workspace ||
-      a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, std::max(a->num_splits, 1)))
-    return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_decode_workspace_size()");
+      a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, std::max(a->num_splits, 1), d))
+    return fail(SINKATTN_ERR_WORKSPACE, "workspace missing or smaller than sinkattn_decode_workspace_size_d()");
   int sms = 0;
   DecodeProblem p{};
   sinkattn_status st = device_info(&p.err, &sms);
@@ -515,12 +519,12 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
     want = std::min<int64_t>({want, 64, std::max<int64_t>(1, maxch / 2)});
     per = (maxch + want - 1) / want;
     while ((maxch + per - 1) / per > 1 &&
-           decode_workspace_bytes(a->nseq, a->Hq, (int)((maxch + per - 1) / per)) > a->workspace_bytes)
+           decode_workspace_bytes(a->nseq, a->Hq, (int)((maxch + per - 1) / per), d) > a->workspace_bytes)
       ++per;
   }
   const int nsplit = (int)((maxch + per - 1) / per);
-  if (a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, nsplit))
-    return fail(SINKATTN_ERR_WORKSPACE, "workspace smaller than sinkattn_decode_workspace_size()");
+  if (a->workspace_bytes < decode_workspace_bytes(a->nseq, a->Hq, nsplit, d))
+    return fail(SINKATTN_ERR_WORKSPACE, "workspace smaller than sinkattn_decode_workspace_size_d()");
   char* ws = static_cast<char*>(a->workspace);
   const size_t n = (size_t)a->nseq * a->Hq * nsplit;
   p.q = static_cast<const __nv_bfloat16*>(a->q);
@@ -539,10 +543,11 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
   p.max_blocks = a->max_blocks_per_seq;
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
+  p.head_dim = d;
   p.window = a->window > 0 ? a->window : 0;
   p.nsplit = nsplit;
   p.split_chunks = (int32_t)per;
-  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / std::sqrt((float)d);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.withhold_copies = withhold_copies();
@@ -554,7 +559,7 @@ sinkattn_status sinkattn_decode(const sinkattn_decode_params* a, void* stream) {
 sinkattn_status sinkattn_decode_exact(const sinkattn_decode_params* a, void* stream) {
   g_message.clear();
   bool empty = false;
-  sinkattn_status st = check_decode(a, &empty, true);
+  sinkattn_status st = check_decode(a, &empty);
   if (st != SINKATTN_OK || empty) return st;
   if (!a->workspace || a->workspace_bytes < 256)
     return fail(SINKATTN_ERR_WORKSPACE, "the exact decode needs a workspace of at least 256 bytes");

@@ -47,23 +47,28 @@ using namespace sm100;
 
 constexpr int kDecThreads = 128;
 constexpr int kChunk = 128;                                // keys per chunk, one per thread
-constexpr uint32_t kChunkBytes = kChunk * kHeadDim * 2;    // 16 KB of K (or V)
+constexpr uint32_t kPanelBytes = kChunk * 64 * 2;          // 128 keys x 64 features: 16 KB
 constexpr int kN = 16;                                     // heads padded to the product's N
+constexpr uint32_t kQPanelBytes = kN * 128;                // 16 heads x 64 features
 constexpr float kLazy = 8.f;                               // log2 headroom of the reference max
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kErrInvalidArg = 1;  // SINKATTN_ERR_INVALID_ARG
 
 // tensor memory columns
-constexpr uint32_t kColO = 0;    // O^T: lanes = output dims (0..63), columns = heads
+constexpr uint32_t kColO = 0;    // O^T: lanes = output dims (0..d-1), columns = heads
 constexpr uint32_t kColS = 16;   // S^T, two buffers of 16: lanes = keys, columns = heads
 constexpr uint32_t kTmemCols = 64;
 
-template <int S>
+// Head_dim 128: a chunk of K (or V) is two 64-feature panels of 128-byte
+// rows, and so is Q; S^T walks both panels, and A = V^T of the second product
+// spans them (M = 128 output dims, the panel distance its leading offset).
+template <int S, int kD>
 struct __align__(1024) DecSmem {
-  uint8_t k[S][kChunkBytes];        // chunk stages, rows of 128 bytes, 128-byte swizzled
+  static constexpr uint32_t kChunkBytes = kPanelBytes * (kD / 64);
+  uint8_t k[S][kChunkBytes];        // chunk stages, panels of 128-byte rows, 128-byte swizzled
   uint8_t v[S][kChunkBytes];
-  uint8_t q[kN * 128];              // [16 heads][64 dims] bf16, 128-byte swizzled (rows >= G zero)
+  uint8_t q[kD / 64][kQPanelBytes]; // [16 heads][64 dims] bf16 per panel, 128-byte swizzled (rows >= G zero)
   uint8_t pt[2][2][kN * 128];       // P^T per buffer: [64-key block][16 heads][64 keys] bf16, swizzled
   float red[4][kN];                 // cross-warp max / sum per head
   int blk[S * (kChunk / 16)];       // physical blocks of the split's first S chunks
@@ -74,8 +79,8 @@ struct __align__(1024) DecSmem {
   int abort;
   int bad;
 };
-template <int S>
-constexpr size_t dec_smem_bytes() { return sizeof(DecSmem<S>) + 1024; }
+template <int S, int kD>
+constexpr size_t dec_smem_bytes() { return sizeof(DecSmem<S, kD>) + 1024; }
 
 // Key range of a sequence in 128-key chunks aligned to the sequence start
 // (the cache block size divides 128), and this split's share: splits take
@@ -111,13 +116,15 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]
       : "memory");
 }
 
-template <int G, int S>
-__global__ void __launch_bounds__(kDecThreads, S == 1 ? 4 : 2)
+template <int G, int S, int kD>
+__global__ void __launch_bounds__(kDecThreads, (S == 1 ? 4 : 2) * 64 / kD)
 decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                     DecodeProblem p) {
   constexpr int kStages = S;
+  constexpr int kPanels = kD / 64;
+  constexpr int kOutWarps = kD / 32;  // warps whose TMEM lanes hold output dims
   extern __shared__ uint8_t smem_raw[];
-  DecSmem<S>& sm = *reinterpret_cast<DecSmem<S>*>(smem_raw + align1024_pad(smem_raw));
+  DecSmem<S, kD>& sm = *reinterpret_cast<DecSmem<S, kD>*>(smem_raw + align1024_pad(smem_raw));
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
   const Range r = split_range(p, b, split);
@@ -128,8 +135,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
     // keys and a single split gets the sink-only row here: o = 0 and
     // lse = S_h (or -inf without sinks).
     if (p.nsplit == 1 && r.L == 0) {
-      for (int i = t; i < G * kHeadDim; i += kDecThreads)
-        p.o[((int64_t)b * p.Hq + kvh * G) * kHeadDim + i] = __float2bfloat16_rn(0.f);
+      for (int i = t; i < G * kD; i += kDecThreads)
+        p.o[((int64_t)b * p.Hq + kvh * G) * kD + i] = __float2bfloat16_rn(0.f);
       if (p.lse && t < G) p.lse[(int64_t)(kvh * G + t) * p.nseq + b] = p.sinks ? p.sinks[kvh * G + t] : -INFINITY;
     }
     return;
@@ -164,11 +171,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
   }
   // Q of the group (rows >= G zero) and P^T rows >= G (zero for good), both
   // in the 128-byte-swizzled K-major layout the products read
-  for (int i = t; i < kN * 8; i += kDecThreads) {
-    const int h = i / 8, cc = i % 8;
+  for (int i = t; i < kN * 8 * kPanels; i += kDecThreads) {
+    const int pi = i / (kN * 8), h = (i / 8) % kN, cc = i % 8;
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (h < G) x = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + kvh * G + h) * kHeadDim + cc * 8);
-    *reinterpret_cast<uint4*>(sm.q + sw128_offset(h, cc)) = x;
+    if (h < G)
+      x = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + kvh * G + h) * kD + 64 * pi + cc * 8);
+    *reinterpret_cast<uint4*>(sm.q[pi] + sw128_offset(h, cc)) = x;
   }
   if constexpr (G < kN) {
     for (int i = t; i < 4 * (kN - G) * 8; i += kDecThreads) {
@@ -205,35 +213,42 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
     if (lane == 0) {
       uint32_t bytes = 0;
       for (int i = 0; i < nbox; ++i)
-        if (box_needed(j0 + i * bs)) bytes += 2u * (uint32_t)bs * kHeadDim * 2u;
+        if (box_needed(j0 + i * bs)) bytes += 2u * (uint32_t)bs * kD * 2u;
       mbar_expect_tx(&sm.full[st], bytes);
     }
     for (int i = 0; i < nbox; ++i) {
       const int pb = __shfl_sync(0xffffffffu, pb_lane, i);
       if (lane == 0 && box_needed(j0 + i * bs)) {
-        tma_load_3d(sm.k[st] + i * bs * 128, &tm_kc, &sm.full[st], 0, kvh, pb * bs);
-        tma_load_3d(sm.v[st] + i * bs * 128, &tm_vc, &sm.full[st], 0, kvh, pb * bs);
+#pragma unroll
+        for (int pi = 0; pi < kPanels; ++pi) {
+          tma_load_3d(sm.k[st] + pi * kPanelBytes + i * bs * 128, &tm_kc, &sm.full[st], 64 * pi, kvh, pb * bs);
+          tma_load_3d(sm.v[st] + pi * kPanelBytes + i * bs * 128, &tm_vc, &sm.full[st], 64 * pi, kvh, pb * bs);
+        }
       }
     }
   };
   // Warp 0: S^T(c) = K Q^T into buffer c & 1 (K-major operands, 4 x K = 16)
   const uint32_t idS = idesc_bf16(128, kN, false, false);
   const uint32_t idO = idesc_bf16(128, kN, true, false);
-  const uint64_t dQ = sdesc_sw128(smem_u32(sm.q), 16, 1024);
+  const uint64_t dQ = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
   auto issue_s = [&](int c) {
     const int st = c % kStages;
     const uint64_t dK = sdesc_sw128(smem_u32(sm.k[st]), 16, 1024);
 #pragma unroll
-    for (int k = 0; k < kHeadDim / 16; ++k)
-      umma_ss_warp(tmem + kColS + 16 * (c & 1), dK + 2 * k, dQ + 2 * k, idS, k > 0);
+    for (int k = 0; k < kD / 16; ++k) {  // +32 bytes per 16 features, panel by panel
+      const uint64_t ok_ = (uint64_t)(k / 4) * (kPanelBytes >> 4) + 2 * (k % 4);
+      const uint64_t oq = (uint64_t)(k / 4) * (kQPanelBytes >> 4) + 2 * (k % 4);
+      umma_ss_warp(tmem + kColS + 16 * (c & 1), dK + ok_, dQ + oq, idS, k > 0);
+    }
     umma_commit_warp(&sm.s_full[c & 1]);
   };
-  // Warp 0: O^T += V^T P^T(c). A = V^T is the V tile read MN-major; its
-  // second 64-row block (M = 128) aliases the first (offset 0), and those
-  // lanes of O^T are never read. B = P^T, two 64-key blocks of 2 KB.
+  // Warp 0: O^T += V^T P^T(c). A = V^T is the V tile read MN-major (M = 128
+  // output rows): at head_dim 128 its two 64-dim panels, at 64 the one panel
+  // twice (leading offset 0), the second copy's lanes of O^T never read.
+  // B = P^T, two 64-key blocks of 2 KB.
   auto issue_pv = [&](int c) {
     const int st = c % kStages, pbuf = c & 1;
-    const uint64_t dV = sdesc_sw128(smem_u32(sm.v[st]), 0, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(sm.v[st]), kD == 128 ? kPanelBytes : 0, 1024);
 #pragma unroll
     for (int k = 0; k < kChunk / 16; ++k) {
       const uint64_t dP = sdesc_sw128(smem_u32(sm.pt[pbuf][k / 4]), 16, 1024) + 2 * (k % 4);
@@ -297,8 +312,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
     if (!valid) {  // stale or never-written V rows must not reach the product (0 * NaN)
       mbar_wait(&sm.full[st], (c / kStages) & 1, g);  // the chunk's copies have landed (done long ago)
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(sm.v[st] + t * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
+      for (int pi = 0; pi < kPanels; ++pi)
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(sm.v[st] + pi * kPanelBytes + t * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     need = __syncthreads_or(need);
     if (sm.abort) break;
@@ -320,7 +337,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
         l_t[gg] *= alpha[gg];
         m_ref[gg] = m_new;
       }
-      if (c > 0 && warp < 2) {  // rescale O^T (lanes 0..63 = dims) once the last product is in
+      if (c > 0 && warp < kOutWarps) {  // rescale O^T (lanes 0..d-1 = dims) once the last product is in
         mbar_wait_warp(&sm.pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, g);
         tc_fence_after();
         uint32_t o[16];
@@ -389,7 +406,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
   }
   __syncthreads();
   ok = ok && !sm.abort;
-  if (ok && warp < 2) {
+  if (ok && warp < kOutWarps) {
     float lsum[G];
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) lsum[gg] = (sm.red[0][gg] + sm.red[1][gg]) + (sm.red[2][gg] + sm.red[3][gg]);
@@ -404,7 +421,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
         const float M = fmaxf(m_ref[gg], sink2);
         const float w = ex2(m_ref[gg] - M);
         const float Z = fmaf(lsum[gg], w, ex2(sink2 - M));
-        p.o[((int64_t)b * p.Hq + h) * kHeadDim + d] = __float2bfloat16_rn(__uint_as_float(o[gg]) * (w / Z));
+        p.o[((int64_t)b * p.Hq + h) * kD + d] = __float2bfloat16_rn(__uint_as_float(o[gg]) * (w / Z));
         if (p.lse && d == 0) p.lse[(int64_t)h * p.nseq + b] = (M + __log2f(Z)) * kLn2;
       }
     } else {
@@ -412,7 +429,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
         const int64_t idx = idx0 + (int64_t)gg * p.nsplit;
-        p.part_o[idx * kHeadDim + d] = __uint_as_float(o[gg]);
+        p.part_o[idx * kD + d] = __uint_as_float(o[gg]);
         if (d == 0) {
           p.part_ml[2 * idx] = m_ref[gg];
           p.part_ml[2 * idx + 1] = lsum[gg];
@@ -444,9 +461,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_cons
   }
 }
 
-// One warp per (sequence, head): two output dims per lane. Only the splits
+// One warp per (sequence, head): d / 32 output dims per lane. Only the splits
 // that hold keys of the sequence wrote partials.
+template <int kD>
 __global__ void __launch_bounds__(32) decode_combine_kernel(DecodeProblem p) {
+  constexpr int kPer = kD / 32;  // consecutive dims per lane
   const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
   const Range r = split_range(p, b, 0);
   if (!length_ok(p, r)) return;  // reported by the split kernel
@@ -457,28 +476,32 @@ __global__ void __launch_bounds__(32) decode_combine_kernel(DecodeProblem p) {
   for (int s = 0; s < ns; ++s) M = fmaxf(M, p.part_ml[2 * (base + s)]);
   const float msub = M == -INFINITY ? 0.f : M;
   float Z = p.sinks ? ex2(sink2 - msub) : 0.f;
-  float o0 = 0.f, o1 = 0.f;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   for (int s = 0; s < ns; ++s) {
     const float w = ex2(p.part_ml[2 * (base + s)] - msub);
     Z = fmaf(p.part_ml[2 * (base + s) + 1], w, Z);
-    const float2 x = *reinterpret_cast<const float2*>(&p.part_o[(base + s) * kHeadDim + 2 * lane]);
-    o0 = fmaf(x.x, w, o0);
-    o1 = fmaf(x.y, w, o1);
+    const float* x = &p.part_o[(base + s) * kD + kPer * lane];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = fmaf(x[e], w, acc[e]);
   }
   const float inv = Z > 0.f ? 1.f / Z : 0.f;
-  reinterpret_cast<uint32_t*>(p.o + ((int64_t)b * p.Hq + h) * kHeadDim)[lane] = pack_bf16(o0 * inv, o1 * inv);
+  uint32_t* out = reinterpret_cast<uint32_t*>(p.o + ((int64_t)b * p.Hq + h) * kD + kPer * lane);
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2) out[e / 2] = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
   if (p.lse && lane == 0) p.lse[(int64_t)h * p.nseq + b] = Z > 0.f ? (msub + __log2f(Z)) * kLn2 : -INFINITY;
 }
 
-template <int G, int S>
+template <int G, int S, int kD>
 cudaError_t launch_split_s(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeProblem& p,
                            cudaStream_t s) {
-  constexpr size_t bytes = dec_smem_bytes<S>();
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)bytes);
+  constexpr size_t bytes = dec_smem_bytes<S, kD>();
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, S, kD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.nsplit, p.Hkv, p.nseq);
-  decode_split_kernel<G, S><<<grid, kDecThreads, bytes, s>>>(mk, mv, p);
+  decode_split_kernel<G, S, kD><<<grid, kDecThreads, bytes, s>>>(mk, mv, p);
   note_launch();
   return cudaGetLastError();
 }
@@ -486,24 +509,28 @@ cudaError_t launch_split_s(const CUtensorMap& mk, const CUtensorMap& mv, const D
 template <int G>
 cudaError_t launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeProblem& p,
                          cudaStream_t s) {
-  return p.split_chunks <= 2 ? launch_split_s<G, 1>(mk, mv, p, s) : launch_split_s<G, 3>(mk, mv, p, s);
+  if (p.head_dim == kHeadDimWide)
+    return p.split_chunks <= 2 ? launch_split_s<G, 1, kHeadDimWide>(mk, mv, p, s)
+                               : launch_split_s<G, 3, kHeadDimWide>(mk, mv, p, s);
+  return p.split_chunks <= 2 ? launch_split_s<G, 1, kHeadDim>(mk, mv, p, s)
+                             : launch_split_s<G, 3, kHeadDim>(mk, mv, p, s);
 }
 
 }  // namespace
 
-size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit) {
+size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit, int32_t head_dim) {
   const size_t n = (size_t)nseq * Hq * nsplit;
-  return ((n * 2 * sizeof(float) + 255) & ~size_t(255)) + n * kHeadDim * sizeof(float);
+  return ((n * 2 * sizeof(float) + 255) & ~size_t(255)) + n * head_dim * sizeof(float);
 }
 
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t s) {
   if (p.nseq == 0) return cudaSuccess;
   CUtensorMap mk, mv;
   const int64_t rows = (int64_t)p.num_blocks * p.block_size;
-  cudaError_t e = make_tmap_bf16_rows(&mk, p.k_cache, p.Hkv, (int)rows, (int64_t)p.Hkv * kHeadDim,
-                                      p.block_size);
+  const int d = p.head_dim;
+  cudaError_t e = make_tmap_bf16_rows(&mk, p.k_cache, p.Hkv, (int)rows, (int64_t)p.Hkv * d, p.block_size, d);
   if (e == cudaSuccess)
-    e = make_tmap_bf16_rows(&mv, p.v_cache, p.Hkv, (int)rows, (int64_t)p.Hkv * kHeadDim, p.block_size);
+    e = make_tmap_bf16_rows(&mv, p.v_cache, p.Hkv, (int)rows, (int64_t)p.Hkv * d, p.block_size, d);
   if (e != cudaSuccess) return e;
   switch (p.Hq / p.Hkv) {
     case 1: e = launch_split<1>(mk, mv, p, s); break;
@@ -515,7 +542,10 @@ cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t s) {
   }
   if (e != cudaSuccess) return e;
   if (p.nsplit == 1) return cudaSuccess;  // the split kernel finished every row
-  decode_combine_kernel<<<dim3(p.Hq, p.nseq), 32, 0, s>>>(p);
+  if (d == kHeadDimWide)
+    decode_combine_kernel<kHeadDimWide><<<dim3(p.Hq, p.nseq), 32, 0, s>>>(p);
+  else
+    decode_combine_kernel<kHeadDim><<<dim3(p.Hq, p.nseq), 32, 0, s>>>(p);
   note_launch();
   return cudaGetLastError();
 }

@@ -58,17 +58,18 @@ struct BwdProblem {
 
 // Decode over a paged KV cache, as the kernels see it.
 struct DecodeProblem {
-  const __nv_bfloat16* q;        // [nseq, Hq, 64]
-  const __nv_bfloat16* k_cache;  // [num_blocks, block_size, Hkv, 64]
+  const __nv_bfloat16* q;        // [nseq, Hq, head_dim]
+  const __nv_bfloat16* k_cache;  // [num_blocks, block_size, Hkv, head_dim]
   const __nv_bfloat16* v_cache;
   const int32_t* block_table;    // [nseq, max_blocks]
   const int32_t* seqlens;        // [nseq]
   const float* sinks;            // null: no sink
-  __nv_bfloat16* o;              // [nseq, Hq, 64]
+  __nv_bfloat16* o;              // [nseq, Hq, head_dim]
   float* lse;                    // [Hq, nseq] or null
   float* part_ml;                // [nseq, Hq, nsplit, 2] workspace: running max (log2 units), sum
-  float* part_o;                 // [nseq, Hq, nsplit, 64] workspace: unnormalised output
+  float* part_o;                 // [nseq, Hq, nsplit, head_dim] workspace: unnormalised output
   int32_t nseq, num_blocks, block_size, max_blocks, Hq, Hkv, window;
+  int32_t head_dim;              // 64 or 128
   int32_t nsplit;                // splits per sequence (grid x)
   int32_t split_chunks;          // 128-key chunks per split
   float scale_log2;              // softmax scale * log2(e)
@@ -178,7 +179,7 @@ cudaError_t prepare_bwd_wide(const BwdProblem& p, BwdWideLaunch* l);
 cudaError_t launch_bwd_wide(const BwdProblem& p, const BwdWideLaunch& l, const TileList& ktiles,
                             int num_sms, cudaStream_t s);
 
-size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit);
+size_t decode_workspace_bytes(int32_t nseq, int32_t Hq, int32_t nsplit, int32_t head_dim);
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t s);
 
 // The limit of the waits inside kernels and the copy-withholding test hook,

@@ -223,11 +223,13 @@ DECODE_CONFIGS = {
     "decode": dict(lengths=_decode_lengths, Hq=64, Hkv=8, block_size=64, seed=6),
     "decode_window": dict(lengths=_decode_lengths, Hq=64, Hkv=8, block_size=64, seed=6,
                           window=128, sink_range=(-4.0, 4.0)),
+    "decode_d128": dict(lengths=_decode_lengths, Hq=64, Hkv=8, block_size=64, seed=6, d=128),
 }
 
 DECODE_DESCRIPTIONS = {
     "decode": "64 seqs L~U[256,8192] Hq=64 Hkv=8 d=64, paged cache of 64-token blocks",
     "decode_window": "as decode, window=128",
+    "decode_d128": "as decode at head_dim 128",
 }
 
 

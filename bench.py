@@ -516,7 +516,7 @@ def decode_bytes(w):
     """Algorithmic bytes of one decode step: the visible keys' K and V rows,
     q and o (bf16), LSE (fp32). Block rounding and the split partials are
     overhead, not counted."""
-    d = HEAD_DIM
+    d = int(w.q.shape[2])
     keys = sum(min(L, w.window) if w.window > 0 else L for L in w.meta["lengths"])
     return keys * w.Hkv * d * 2 * 2 + w.nseq * w.Hq * (2 * d * 2 + 4)
 
@@ -525,7 +525,7 @@ def decode_config_record(w, name):
     from attention_learnable_sinks_gb300.workloads import DECODE_DESCRIPTIONS
     return {"workload": f"{name}: {DECODE_DESCRIPTIONS[name]}", "nseq": w.nseq,
             "cached_tokens": sum(w.meta["lengths"]), "Hq": w.Hq, "Hkv": w.Hkv,
-            "head_dim": HEAD_DIM, "block_size": w.block_size, "window": w.window,
+            "head_dim": int(w.q.shape[2]), "block_size": w.block_size, "window": w.window,
             "l2": L2_NOTE,
             "byte_convention": "visible K,V rows + q + o + lse per step"}
 
@@ -549,7 +549,7 @@ def oracle_decode_sample(w, seqs):
     odec.decode(q, kc, vc, w.block_table.numpy()[seqs], w.seqlens.numpy()[seqs], w.sinks.numpy(),
                 window=w.window, scale=w.scale)
     dt = time.perf_counter() - t0
-    d = HEAD_DIM
+    d = int(w.q.shape[2])
     lens = [w.meta["lengths"][b] for b in seqs]
     keys = sum(min(L, w.window) if w.window > 0 else L for L in lens)
     return dt, keys * w.Hkv * d * 4 + len(seqs) * w.Hq * (4 * d + 4)
@@ -595,7 +595,7 @@ def run_decode(args):
     table, lens, s = w.block_table.to(device), w.seqlens.to(device), w.sinks.to(device)
     o = torch.empty_like(q)
     lse = torch.empty(w.Hq, w.nseq, dtype=torch.float32, device=device)
-    ws = torch.empty(_binding.lib().sinkattn_decode_workspace_size(w.nseq, w.Hq, 64),
+    ws = torch.empty(_binding.lib().sinkattn_decode_workspace_size_d(w.nseq, w.Hq, 64, int(w.q.shape[2])),
                      dtype=torch.uint8, device=device)
     flush = L2Flush(device)
     nbytes = decode_bytes(w)
@@ -701,7 +701,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", default="dense",
                     choices=("tiny", "dense", "window", "varlen", "long", "long_window",
-                             "dense_d128", "decode", "decode_window"))
+                             "dense_d128", "decode", "decode_window", "decode_d128"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
                     help="backward with dq summed in a fixed order (query-stationary dq pass)")

@@ -25,8 +25,7 @@
  * window of W keys is the W most recent keys, the diagonal included.
  * Sequences never see each other.
  *
- * Data layout (all device memory, caller-owned), d = head_dim (64 or 128;
- * sinkattn_decode takes 64 only):
+ * Data layout (all device memory, caller-owned), d = head_dim (64 or 128):
  *   q        bf16 [total, Hq,  d], token row stride q_row_stride elements
  *   k, v     bf16 [total, Hkv, d], token row strides k_row_stride, v_row_stride
  *   o, dout, dq   bf16 [total, Hq, d] contiguous
@@ -216,7 +215,7 @@ SINKATTN_API sinkattn_status sinkattn_bwd_static_workspace(const sinkattn_bwd_pa
  * The keys are split into up to num_splits ranges processed side by side;
  * the partial results are merged with the sink in a second kernel.
  *
- * Layouts (d = head_dim: 64; sinkattn_decode_exact also takes 128):
+ * Layouts (d = head_dim: 64 or 128):
  *   q            bf16 [nseq, Hq, d] contiguous
  *   k_cache,     bf16 [num_blocks, block_size, Hkv, d] contiguous; logical
  *   v_cache      block i of sequence b is physical block block_table[b][i]
@@ -248,14 +247,19 @@ typedef struct sinkattn_decode_params {
   int32_t max_blocks_per_seq;  /* columns of block_table                       */
   int32_t Hq;
   int32_t Hkv;
-  int32_t head_dim;            /* 64 (sinkattn_decode_exact: 64 or 128)       */
+  int32_t head_dim;            /* d: 64 or 128                                 */
   int32_t window;              /* <= 0: every key; W > 0: the last W keys      */
   int32_t num_splits;          /* key ranges per sequence, 1..64; 0 = choose    */
   float softmax_scale;         /* <= 0 selects 1/sqrt(head_dim)                */
 } sinkattn_decode_params;
 
-/* Workspace bytes for a decode problem (0 on bad input). */
+/* Workspace bytes for a decode problem (0 on bad input): the split partials,
+ * (max, sum) and an unnormalised output row per (sequence, head, split).
+ * sinkattn_decode_workspace_size is the head_dim 64 size;
+ * sinkattn_decode_workspace_size_d takes the head_dim (64 or 128). */
 SINKATTN_API size_t sinkattn_decode_workspace_size(int32_t nseq, int32_t Hq, int32_t num_splits);
+SINKATTN_API size_t sinkattn_decode_workspace_size_d(int32_t nseq, int32_t Hq, int32_t num_splits,
+                                                     int32_t head_dim);
 
 /* Enqueue the decode on `stream`. num_splits = 0 picks the split count from
  * the shape (nseq, Hkv, max_blocks_per_seq * block_size) and the SM count;
@@ -277,8 +281,8 @@ SINKATTN_API sinkattn_status sinkattn_decode(const sinkattn_decode_params* param
  * counter, cleared by the call). Cache slots past a sequence's last key and
  * blocks wholly before its window are not read. Block indices out of range
  * set SINKATTN_ERR_INVALID_ARG in the device error word and read as zeros.
- * head_dim may be 128 here (the training forward's head_dim 128 kernel, in
- * its decode form). */
+ * At head_dim 128 it is the training forward's head_dim 128 kernel in its
+ * decode form. */
 SINKATTN_API sinkattn_status sinkattn_decode_exact(const sinkattn_decode_params* params, void* stream);
 
 /* Static description of a status code; never NULL. */

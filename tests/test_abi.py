@@ -68,6 +68,18 @@ def test_param_struct_field_offsets_match(tmp_path):
         assert int(got[cname]) == ctypes.sizeof(cls), cname
 
 
+def test_decode_workspace_sizes():
+    lib = _binding.lib()
+    w64 = lib.sinkattn_decode_workspace_size(5, 64, 8)
+    assert w64 == lib.sinkattn_decode_workspace_size_d(5, 64, 8, 64)
+    # (max, sum) pairs, then one output row per (sequence, head, split)
+    n = 5 * 64 * 8
+    assert w64 == ((n * 8 + 255) // 256) * 256 + n * 64 * 4
+    assert lib.sinkattn_decode_workspace_size_d(5, 64, 8, 128) == ((n * 8 + 255) // 256) * 256 + n * 128 * 4
+    assert lib.sinkattn_decode_workspace_size_d(5, 64, 8, 96) == 0
+    assert lib.sinkattn_decode_workspace_size_d(5, 64, 65, 64) == 0
+
+
 def test_workspace_sizes():
     lib = _binding.lib()
     f = lib.sinkattn_fwd_workspace_size(4, 8192, 64, 8, 64)
@@ -184,7 +196,8 @@ def _decode_params(**kw):
 
 
 @pytest.mark.parametrize("change,status", [
-    ({"head_dim": 128}, 2),
+    ({"head_dim": 96}, 2),
+    ({"head_dim": 128, "block_size": 8}, 2),   # head_dim 128 passes; the block size does not
     ({"Hq": 6, "Hkv": 2}, 2),      # group of 3
     ({"Hq": 64, "Hkv": 2}, 2),     # group of 32
     ({"Hkv": 3}, 1),

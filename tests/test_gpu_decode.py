@@ -73,6 +73,15 @@ CASES = [
     ("peaked_logits", [900, 1500], 8, 1, 16, 0, 0, {"qk_std": 2.0, "sink_range": (-10.0, 10.0)}),
     ("sinks_minus30", [450, 33], 4, 2, 64, 0, 0, {"odd_head_sink": -30.0}),
     ("g2_window_long", [8192, 4000], 4, 2, 128, 1000, 0, {}),
+    # head_dim 128: two 64-feature panels per cache block, M = 128 output dims
+    ("d128_basic_bs16", [1, 5, 127, 128, 129, 1000], 8, 2, 16, 0, 0, {"d": 128}),
+    ("d128_empty_and_one_bs32", [0, 1, 0, 2, 33], 4, 4, 32, 0, 0, {"d": 128}),
+    ("d128_g16_bs64", [700, 64, 4096], 16, 1, 64, 0, 0, {"d": 128}),
+    ("d128_window300_5splits", [299, 300, 301, 2000], 8, 1, 32, 300, 5, {"d": 128}),
+    ("d128_one_split", [5000, 17], 8, 2, 64, 0, 1, {"d": 128}),
+    ("d128_64_splits_some_empty", [5000, 3], 8, 2, 16, 0, 64, {"d": 128}),
+    ("d128_peaked_bs128", [900, 1500], 8, 1, 128, 0, 0,
+     {"d": 128, "qk_std": 2.0, "sink_range": (-10.0, 10.0)}),
 ]
 
 
