@@ -60,8 +60,9 @@ def test_forward_and_backward_waits_run_out_then_recover(cuda_lib, d):
         compare_full(w, run_cuda(w, deterministic=det), ref)
 
 
-def test_decode_waits_run_out_then_recover(cuda_lib):
-    w = make_decode("watchdog_decode", [200, 1000, 3000], 8, 2, block_size=64, seed=32)
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_waits_run_out_then_recover(cuda_lib, d):
+    w = make_decode(f"watchdog_decode_d{d}", [200, 1000, 3000], 8, 2, block_size=64, seed=32, d=d)
     dev = "cuda"
     args = [t.to(dev) for t in (w.q, w.k_cache, w.v_cache, w.block_table, w.seqlens)]
     s = w.sinks.to(dev)
@@ -70,6 +71,7 @@ def test_decode_waits_run_out_then_recover(cuda_lib):
     assert _binding.device_error(reset=True) == 0
     for splits in (1, 4):
         _expect_timeout(lambda: api.decode(*args, s, num_splits=splits))
+    _expect_timeout(lambda: api.decode(*args, s, exact=True))
     o, lse = api.decode(*args, s, num_splits=1)
     torch.cuda.synchronize()
     assert _binding.device_error(reset=True) == 0
