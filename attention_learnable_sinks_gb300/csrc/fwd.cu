@@ -254,17 +254,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t nq = 0, nk = 0, nv = 0;
-      // This CTA's share of the backward's dq accumulator, cleared one chunk
-      // per key-tile load (the forward leaves memory bandwidth unused) and the
-      // rest after its last unit.
+      // This CTA's share of the backward's dq accumulator, cleared a few
+      // chunks per key-tile load (the forward leaves memory bandwidth unused)
+      // and the rest after its last unit. The chunks per load come from the
+      // key-tile loads a CTA can expect (the list's total cost x heads / CTAs),
+      // so that short units (a narrow window) still spread the clear over
+      // the whole kernel instead of leaving it to the end.
       int64_t clr = 0, clr_end = 0;
+      int per_load = 1;
       if (!kDecode && p.clear) {
         const int64_t n16 = p.clear_bytes / 16;
         clr = n16 * blockIdx.x / gridDim.x * 16;
         clr_end = n16 * (blockIdx.x + 1) / gridDim.x * 16;
+        const int64_t loads = (int64_t)meta[2] * p.Hq / gridDim.x;  // expected, this CTA
+        const int64_t chunks = (clr_end - clr + kClearChunk - 1) / kClearChunk;
+        // done by the last expected load (what a CTA with fewer loads leaves
+        // goes after its last unit); at most 8 chunks per load
+        per_load = (int)std::min<int64_t>(8, std::max<int64_t>(1, (chunks + loads - 1) / std::max<int64_t>(loads, 1)));
       }
       auto clear_some = [&]() {
-        if (clr < clr_end) {
+        for (int r = 0; r < per_load && clr < clr_end; ++r) {
           const int64_t left = clr_end - clr;
           const uint32_t n = left < (int64_t)kClearChunk ? (uint32_t)left : kClearChunk;
           bulk_store(p.clear + clr, sm.zeros, n);

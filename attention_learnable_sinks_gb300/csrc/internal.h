@@ -88,8 +88,8 @@ struct PagedKV {
 };
 
 // Tile work list in the workspace: meta[0] = number of items, meta[1] = the
-// next item to hand out (work stealing), items[] = {sequence, tile} sorted by
-// decreasing cost.
+// next item to hand out (work stealing), meta[2] = the items' total cost,
+// items[] = {sequence, tile} sorted by decreasing cost.
 struct TileList {
   int32_t* meta;
   int2* items;

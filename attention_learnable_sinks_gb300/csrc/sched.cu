@@ -68,9 +68,13 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
   __shared__ int hist[kBuckets];
   __shared__ int warp_sums[kThreads / 32];
   __shared__ int bad;
+  __shared__ unsigned long long total_cost;
   const int tid = threadIdx.x;
   for (int i = tid; i < kBuckets; i += kThreads) hist[i] = 0;
-  if (tid == 0) bad = (nseq >= 0 && (cu[0] != 0 || cu[nseq] != total)) ? 1 : 0;
+  if (tid == 0) {
+    bad = (nseq >= 0 && (cu[0] != 0 || cu[nseq] != total)) ? 1 : 0;
+    total_cost = 0ull;
+  }
   __syncthreads();
 
   // pass 1: validate lengths, histogram of costs; a warp per sequence, its
@@ -83,14 +87,20 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
       continue;
     }
     const int nt = (L + kTile - 1) / kTile;
-    for (int t = lane; t < nt; t += 32)
-      atomicAdd(&hist[bucket_of(seq_major, levels, b, tile_cost(by_keys, causal, window, L, t))], 1);
+    unsigned long long cost_sum = 0ull;
+    for (int t = lane; t < nt; t += 32) {
+      const int cost = tile_cost(by_keys, causal, window, L, t);
+      atomicAdd(&hist[bucket_of(seq_major, levels, b, cost)], 1);
+      cost_sum += (unsigned long long)cost;
+    }
+    if (cost_sum) atomicAdd(&total_cost, cost_sum);
   }
   __syncthreads();
   if (bad) {
     if (tid == 0) {
       meta[0] = 0;
       meta[1] = 0;
+      meta[2] = 0;
       atomicCAS(err, 0, 1 /* SINKATTN_ERR_INVALID_ARG */);
     }
     return;
@@ -138,6 +148,7 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
     if (tid == 0) {
       meta[0] = 0;
       meta[1] = 0;
+      meta[2] = 0;
       atomicCAS(err, 0, 4 /* SINKATTN_ERR_WORKSPACE */);
     }
     return;
@@ -156,6 +167,9 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
   if (tid == 0) {
     meta[0] = n_items;
     meta[1] = 0;
+    // total cost (key tiles seen by the query tiles, or query tiles seeing
+    // the key tiles): the forward paces its clearing copies by it
+    meta[2] = (int32_t)min(total_cost, 0x7fffffffull);
   }
 }
 
