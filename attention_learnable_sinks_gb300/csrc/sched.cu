@@ -93,7 +93,11 @@ build_tile_list_kernel(const int32_t* __restrict__ cu, int nseq, int total, int 
       atomicAdd(&hist[bucket_of(seq_major, levels, b, cost)], 1);
       cost_sum += (unsigned long long)cost;
     }
-    if (cost_sum) atomicAdd(&total_cost, cost_sum);
+    // one shared-memory add per warp (every lane adding its own costs a
+    // measurable few microseconds of contention)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cost_sum += __shfl_xor_sync(0xffffffffu, cost_sum, o);
+    if (lane == 0 && cost_sum) atomicAdd(&total_cost, cost_sum);
   }
   __syncthreads();
   if (bad) {
