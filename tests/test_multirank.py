@@ -35,9 +35,9 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _workload():
+def _workload(d=64):
     # ragged lengths, an empty and a length-1 sequence, GQA 4:1, W = 2 head shards
-    return make("multirank", [150, 37, 0, 260, 1, 90], 8, 2, seed=41, sink_range=(-3.0, 3.0))
+    return make("multirank", [150, 37, 0, 260, 1, 90], 8, 2, seed=41, sink_range=(-3.0, 3.0), d=d)
 
 
 def _f64(t):
@@ -95,8 +95,8 @@ def _entry(fn, rank, port, q, *args):
             dist.destroy_process_group()
 
 
-def _rank_data_parallel(rank):
-    w = _workload()
+def _rank_data_parallel(rank, d=64):
+    w = _workload(d)
     lens = (w.cu_seqlens[1:] - w.cu_seqlens[:-1]).tolist()
     parts = sharding.partition_sequences(lens, WORLD, w.causal, w.window)
     tok, cu, maxlen = sharding.shard_tokens(w.cu_seqlens.tolist(), parts[rank])
@@ -109,10 +109,11 @@ def _rank_data_parallel(rank):
     return {"rank": rank, "tok": tok.numpy(), "seqs": parts[rank], **r}
 
 
-def test_data_parallel_split_matches_whole_batch():
-    w = _workload()
+@pytest.mark.parametrize("d", [64, 128])
+def test_data_parallel_split_matches_whole_batch(d):
+    w = _workload(d)
     ref = _reference(w)
-    res = _spawn(_rank_data_parallel)
+    res = _spawn(_rank_data_parallel, d)
     seen = sorted(b for r in res for b in r["seqs"])
     assert seen == list(range(w.nseq)), "every sequence on exactly one rank"
     for r in res:
@@ -126,9 +127,9 @@ def test_data_parallel_split_matches_whole_batch():
     assert not np.allclose(res[0]["dsinks"], ref["dsinks"])
 
 
-def _rank_head_split(rank):
+def _rank_head_split(rank, d=64):
     import torch.distributed as dist
-    w = _workload()
+    w = _workload(d)
     splits = sharding.token_split(w.total, WORLD)
     t0 = sum(splits[:rank])
     sl = slice(t0, t0 + splits[rank])
@@ -150,10 +151,11 @@ def _rank_head_split(rank):
             bool((ds.numpy()[np.r_[0:hs.start, hs.stop:w.Hq]] == 0).all())}
 
 
-def test_head_split_all_to_all_matches_single_process():
-    w = _workload()
+@pytest.mark.parametrize("d", [64, 128])
+def test_head_split_all_to_all_matches_single_process(d):
+    w = _workload(d)
     ref = _reference(w)
-    res = _spawn(_rank_head_split)
+    res = _spawn(_rank_head_split, d)
     assert [r["slice"] for r in res] == [(0, 269), (269, 538)]
     for r in res:
         a, b = r["slice"]
