@@ -27,7 +27,7 @@ def _full_sequence_last_rows(w):
     cu[1:] = np.cumsum(lens)
     total = int(cu[-1])
     rng = np.random.default_rng(0)
-    q = rng.standard_normal((total, w.Hq, 64))
+    q = rng.standard_normal((total, w.Hq, w.q.shape[2]))
     for b, L in enumerate(lens):
         if L:
             q[cu[b] + L - 1] = _f64(w.q[b])
@@ -37,14 +37,16 @@ def _full_sequence_last_rows(w):
     return ref, cu
 
 
-@pytest.mark.parametrize("lengths,Hq,Hkv,bs,window", [
-    ([1, 5, 130, 300], 8, 2, 16, 0),
-    ([17, 129, 256], 4, 1, 128, 0),
-    ([200, 64, 9], 8, 4, 32, 7),
-    ([300, 129], 4, 2, 64, 128),
+@pytest.mark.parametrize("lengths,Hq,Hkv,bs,window,d", [
+    ([1, 5, 130, 300], 8, 2, 16, 0, 64),
+    ([17, 129, 256], 4, 1, 128, 0, 64),
+    ([200, 64, 9], 8, 4, 32, 7, 64),
+    ([300, 129], 4, 2, 64, 128, 64),
+    ([1, 5, 130, 300], 8, 2, 16, 0, 128),
+    ([300, 129], 4, 2, 64, 128, 128),
 ])
-def test_matches_last_row_of_c_oracle(lengths, Hq, Hkv, bs, window):
-    w = make_decode("pin", lengths, Hq, Hkv, bs, seed=11, window=window)
+def test_matches_last_row_of_c_oracle(lengths, Hq, Hkv, bs, window, d):
+    w = make_decode("pin", lengths, Hq, Hkv, bs, seed=11, window=window, d=d)
     o, lse = odec.decode(_f64(w.q), _f64(w.k_cache), _f64(w.v_cache), w.block_table.numpy(),
                          w.seqlens.numpy(), w.sinks.numpy(), window=window, scale=w.scale)
     ref, cu = _full_sequence_last_rows(w)
