@@ -59,6 +59,7 @@ constexpr int kThreads = 192;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr uint32_t kPanelBytes = kTile * 64 * 2;  // 128 rows x 64 features of bf16
+constexpr uint32_t kOPanelBytes = 32 * 128;        // O staging: 32 rows x 64 features of bf16
 constexpr uint32_t kColS = 0, kColP = 128;
 // per head dim: tile bytes, tensor-memory columns, O's column, CTAs per SM
 template <int kD>
@@ -89,7 +90,7 @@ struct __align__(1024) Smem {
   uint8_t q[kTileBytes];
   uint8_t k[kKStages][kTileBytes];
   uint8_t v[kVStages][kTileBytes];
-  uint8_t ostage[4][32 * kD * 2];  // per softmax warp: its 32 rows of O (bf16), 16-byte chunks swizzled
+  uint8_t ostage[4][32 * kD * 2];  // per softmax warp: its 32 rows of O (bf16), 64-feature panels, swizzled
   uint8_t zeros[kClearChunk];   // source of the bulk copies that clear the backward's dq accumulator
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
@@ -184,6 +185,19 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// TMA tensor store of a shared-memory box (no commit; see bulk_commit_group).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 
 // Wait that ignores the abort flag (still time-bounded): used only to drain
 // copies / products this thread issued before the CTA exits.
@@ -196,8 +210,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 template <bool kDecode, int kD>
 __global__ void __launch_bounds__(kThreads, Cfg<kD>::kCtasPerSm)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_v, Problem p, PagedKV kv,
-           const int2* __restrict__ items, int32_t* __restrict__ meta) {
+           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, Problem p,
+           PagedKV kv, const int2* __restrict__ items, int32_t* __restrict__ meta) {
   static_assert(kD == 64 || kD == 128, "head_dim 64 or 128");
   using C = Cfg<kD>;
   constexpr uint32_t kTileBytes = C::kTileBytes;
@@ -616,27 +630,47 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         continue;
       }
-      // O rows through shared memory, so that each store instruction writes
-      // whole rows (four of 128 bytes, or two of 256) instead of 16 bytes of
-      // 32 rows
-      constexpr int kRowBytes = kD * 2, kChunks = kD / 8, kRowsPerStore = 32 / kChunks;
+      // O rows through shared memory, as 64-feature panels of 32 rows x 128
+      // bytes in the 128-byte swizzle TMA uses. A warp whose 32 rows all
+      // belong to the sequence hands them to one asynchronous TMA store per
+      // panel and goes on to its next unit; a warp with rows past the
+      // sequence end (they are the next sequence's) stores its valid rows
+      // itself, four whole rows per instruction.
+      constexpr int kChunks = kD / 8;
       uint8_t* ost = sm.ostage[quarter];
+      if (lane == 0) bulk_wait_read0();  // this warp's previous store has read the staging rows
+      __syncwarp();
 #pragma unroll
       for (int c = 0; c < kChunks; ++c)
-        *reinterpret_cast<uint4*>(ost + lane * kRowBytes + ((c ^ (lane & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(ost + (c / 8) * kOPanelBytes + lane * 128 + (((c % 8) ^ (lane & 7)) << 4)) =
             make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-      __syncwarp();
+      if (32 * quarter + 31 < nrows) {
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
 #pragma unroll
-      for (int k = 0; k < 32 / kRowsPerStore; ++k) {
-        const int rr = kRowsPerStore * k + lane / kChunks, c = lane % kChunks;  // row of this warp, 16-byte chunk
-        const uint4 x = *reinterpret_cast<const uint4*>(ost + rr * kRowBytes + ((c ^ (rr & 7)) << 4));
-        if (32 * quarter + rr < nrows)
-          reinterpret_cast<uint4*>(p.o + ((int64_t)(row0 + 32 * quarter + rr) * p.Hq + h) * kD)[c] = x;
+          for (int pi = 0; pi < C::kPanels; ++pi)
+            tma_store_3d(&tm_o, ost + pi * kOPanelBytes, 64 * pi, h, row0 + 32 * quarter);
+          bulk_commit_group();
+        }
+      } else {
+        __syncwarp();
+#pragma unroll
+        for (int pi = 0; pi < C::kPanels; ++pi) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3), c = lane & 7;  // row of this warp, 16-byte chunk
+            const uint4 x = *reinterpret_cast<const uint4*>(ost + pi * kOPanelBytes + rr * 128 + ((c ^ (rr & 7)) << 4));
+            if (32 * quarter + rr < nrows)
+              reinterpret_cast<uint4*>(p.o + ((int64_t)(row0 + 32 * quarter + rr) * p.Hq + h) * kD)[8 * pi + c] = x;
+          }
+        }
+        __syncwarp();
       }
-      __syncwarp();
       if (p.lse && r < nrows)
         p.lse[(int64_t)h * p.total + row0 + r] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
+    if (lane == 0) bulk_wait_all();  // this warp's O stores are complete before the CTA exits
   }
 
   tc_fence_before();
@@ -654,6 +688,7 @@ cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l) {
   cudaError_t e = make_tmap_bf16_rows(&l->q, p.q, p.Hq, p.total, p.q_stride, kTile, d);
   if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->k, p.k, p.Hkv, p.total, p.k_stride, kTile, d);
   if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.v, p.Hkv, p.total, p.v_stride, kTile, d);
+  if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->o, p.o, p.Hq, p.total, (int64_t)p.Hq * d, 32, d);
   if (e != cudaSuccess) return e;
   if (d == 128)
     return cudaFuncSetAttribute(fwd_kernel<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -669,10 +704,10 @@ cudaError_t launch_fwd(const Problem& p, const FwdLaunch& l, const TileList& qti
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * per_sm);
   if (grid <= 0) return cudaSuccess;
   if (p.head_dim == 128)
-    fwd_kernel<false, 128><<<grid, kThreads, smem_bytes<128>(), s>>>(l.q, l.k, l.v, p, PagedKV{},
+    fwd_kernel<false, 128><<<grid, kThreads, smem_bytes<128>(), s>>>(l.q, l.k, l.v, l.o, p, PagedKV{},
                                                                      qtiles.items, qtiles.meta);
   else
-    fwd_kernel<false, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(l.q, l.k, l.v, p, PagedKV{},
+    fwd_kernel<false, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(l.q, l.k, l.v, l.o, p, PagedKV{},
                                                                    qtiles.items, qtiles.meta);
   note_launch();
   return cudaGetLastError();
@@ -699,10 +734,11 @@ cudaError_t launch_decode_exact(const Problem& p, const PagedKV& kv, const void*
   const int per_sm = d == 128 ? Cfg<128>::kCtasPerSm : Cfg<64>::kCtasPerSm;
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * per_sm);
   if (grid <= 0) return cudaSuccess;
+  // (the decode form writes its rows itself: the O map argument is unused)
   if (d == 128)
-    fwd_kernel<true, 128><<<grid, kThreads, smem_bytes<128>(), s>>>(mq, mk, mv, p, kv, nullptr, counter);
+    fwd_kernel<true, 128><<<grid, kThreads, smem_bytes<128>(), s>>>(mq, mk, mv, mq, p, kv, nullptr, counter);
   else
-    fwd_kernel<true, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(mq, mk, mv, p, kv, nullptr, counter);
+    fwd_kernel<true, 64><<<grid, kThreads, smem_bytes<64>(), s>>>(mq, mk, mv, mq, p, kv, nullptr, counter);
   note_launch();
   return cudaGetLastError();
 }

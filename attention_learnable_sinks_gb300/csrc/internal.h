@@ -146,7 +146,7 @@ cudaError_t launch_build_tile_list(const Problem& p, int by_keys, int seq_major,
 // launch, so that its kernels go out back to back (host-side preparation
 // between two launches would leave the GPU idle).
 struct FwdLaunch {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, o;  // o: boxes of 32 rows x 64 features (the epilogue's TMA stores)
 };
 struct BwdLaunch {
   CUtensorMap q, k, v, dout, dq;
