@@ -193,15 +193,7 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
       "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
+
 
 // kDQ = false: the deterministic mode's instantiation, without the dQ
 // products and read-out (dq then comes from the query-stationary pass).
@@ -778,6 +770,8 @@ cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l) {
   if (e == cudaSuccess) e = make_tmap_bf16_rows(&l->v, p.f.v, p.f.Hkv, p.f.total, p.f.v_stride, kTile, d);
   if (e == cudaSuccess)
     e = make_tmap_bf16_rows(&l->dout, p.dout, p.f.Hq, p.f.total, (int64_t)p.f.Hq * d, kTile, d);
+  if (e == cudaSuccess)  // bf16 dq, written by the dq pass in 32-row boxes of half the features
+    e = make_tmap_bf16_box(&l->dqo, p.dq, p.f.Hq, p.f.total, (int64_t)p.f.Hq * d, d, d / 2, 32);
   if (e != cudaSuccess || d != kHeadDim) return e;
   e = make_tmap_f32_rows(&l->dq, p.dq_acc, p.f.Hq, p.f.total);
   if (e != cudaSuccess) return e;

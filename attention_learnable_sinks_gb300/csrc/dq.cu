@@ -76,6 +76,9 @@ struct __align__(1024) Smem {
   uint64_t kv_full[kKVStages], kv_empty[kKVStages];
   uint64_t sdp_full, sdp_empty, ds_full[2], ds_free[2];
   uint64_t dq_full[Cfg<kD>::kDQBufs], dq_empty[Cfg<kD>::kDQBufs], drain;
+  // dq staging: per softmax warp, its 32 rows x kD/2 columns (bf16), in the
+  // swizzle of the TMA store that writes them (64 or 128 bytes per row)
+  alignas(1024) uint8_t dqst[8][32 * kD];
   uint64_t sched_full[kSchedSlots], sched_empty[kSchedSlots];
   int32_t sched_unit[kSchedSlots];  // work unit handed out, -1 = no more work
   Unit sched_u[kSchedSlots];         // ... decoded by the producer
@@ -116,7 +119,8 @@ template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-          BwdProblem bp, const int2* __restrict__ items, int32_t* __restrict__ meta) {
+          const __grid_constant__ CUtensorMap tm_dqo, BwdProblem bp, const int2* __restrict__ items,
+          int32_t* __restrict__ meta) {
   using C = Cfg<kD>;
   constexpr uint32_t kTileBytes = C::kTileBytes;
   constexpr int kQBufs = C::kQBufs, kKVStages = C::kKVStages, kDQBufs = C::kDQBufs;
@@ -352,7 +356,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       int64_t orow;  // output row (token * Hq + head)
       int slot;
       bool valid, any;
-    } pend{0, 0, false, false};
+      int row0, h;   // the warp's first row (token) and the head, for its TMA store
+    } pend{0, 0, false, false, 0, 0};
+    uint8_t* stage = sm.dqst[warp - 2];
     bool has_pend = false;
     auto epilogue = [&]() -> bool {  // dq = bf16(scale * dQ), columns kD/2 wg .. kD/2 (wg + 1)
       constexpr int kHalf = kD / 2;
@@ -369,15 +375,34 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       mbar_arrive(&sm.dq_empty[dqb]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sched_empty[pend.slot]);  // the slot is no longer read
-      if (pend.valid) {
-        const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
-        uint32_t ob[kHalf / 2];
+      const float sc = p.scale;  // dq = scale * sum_j dS_ij k_j
+      uint32_t ob[kHalf / 2];
 #pragma unroll
-        for (int e = 0; e < kHalf / 2; ++e)
-          ob[e] = pend.any ? pack_bf16(__uint_as_float(a[2 * e]) * sc, __uint_as_float(a[2 * e + 1]) * sc) : 0u;
+      for (int e = 0; e < kHalf / 2; ++e)
+        ob[e] = pend.any ? pack_bf16(__uint_as_float(a[2 * e]) * sc, __uint_as_float(a[2 * e + 1]) * sc) : 0u;
+      // rows through shared memory: a warp whose 32 rows all exist hands them
+      // to one TMA store and goes on; a tail warp stores its valid rows itself
+      constexpr int kChunks = kHalf / 8;  // 16-byte chunks per row: 4 or 8
+      auto swz = [&](int row, int c) {    // the TMA swizzle of a row of kChunks 16-byte chunks
+        return (uint32_t)(row * kChunks * 16) +
+               ((uint32_t)(kChunks == 8 ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3))) << 4);
+      };
+      if (__all_sync(0xffffffffu, pend.valid)) {
+        if (lane == 0) bulk_wait_read0();  // the previous store has read the staging rows
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+          *reinterpret_cast<uint4*>(stage + swz(lane, c)) = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_dqo, stage, kHalf * wg, pend.h, pend.row0);
+          bulk_commit();
+        }
+      } else if (pend.valid) {
         uint4* dst = reinterpret_cast<uint4*>(bp.dq + pend.orow * kD + kHalf * wg);
 #pragma unroll
-        for (int c = 0; c < kHalf / 8; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+        for (int c = 0; c < kChunks; ++c) dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
       }
       has_pend = false;
       return true;
@@ -445,10 +470,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       if (ok && has_pend) ok = epilogue();
       for (int jj = 1; jj < n && ok; ++jj) ok = tile(jj);
       if (!ok) break;
-      pend = Pending{(int64_t)(uv.base + i) * p.Hq + uv.h, slot, valid, n > 0};
+      pend = Pending{(int64_t)(uv.base + i) * p.Hq + uv.h, slot, valid, n > 0,
+                     uv.base + uv.r0 + 32 * quarter, uv.h};
       has_pend = true;
     }
     if (ok && has_pend) epilogue();  // the last unit
+    if (lane == 0) bulk_wait0();     // this warp's dq stores are complete before the CTA exits
   }
 
   tc_fence_before();
@@ -475,10 +502,10 @@ cudaError_t launch_bwd_dq(const BwdProblem& p, const BwdLaunch& l, const TileLis
   const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms);
   if (grid <= 0) return cudaSuccess;
   if (p.f.head_dim == kHeadDimWide)
-    dq_kernel<kHeadDimWide><<<grid, kThreads, smem_bytes<kHeadDimWide>(), s>>>(l.q, l.k, l.v, l.dout, p,
+    dq_kernel<kHeadDimWide><<<grid, kThreads, smem_bytes<kHeadDimWide>(), s>>>(l.q, l.k, l.v, l.dout, l.dqo, p,
                                                                              qtiles.items, qtiles.meta);
   else
-    dq_kernel<kHeadDim><<<grid, kThreads, smem_bytes<kHeadDim>(), s>>>(l.q, l.k, l.v, l.dout, p,
+    dq_kernel<kHeadDim><<<grid, kThreads, smem_bytes<kHeadDim>(), s>>>(l.q, l.k, l.v, l.dout, l.dqo, p,
                                                                      qtiles.items, qtiles.meta);
   note_launch();
   return cudaGetLastError();

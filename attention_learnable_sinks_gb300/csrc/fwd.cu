@@ -182,22 +182,7 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// TMA tensor store of a shared-memory box (no commit; see bulk_commit_group).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
+__device__ __forceinline__ void bulk_wait_all() { bulk_wait0(); }
 
 // Wait that ignores the abort flag (still time-bounded): used only to drain
 // copies / products this thread issued before the CTA exits.
@@ -651,7 +636,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 #pragma unroll
           for (int pi = 0; pi < C::kPanels; ++pi)
             tma_store_3d(&tm_o, ost + pi * kOPanelBytes, 64 * pi, h, row0 + 32 * quarter);
-          bulk_commit_group();
+          bulk_commit();
         }
       } else {
         __syncwarp();

@@ -130,6 +130,12 @@ cudaError_t make_tmap_bf16_rows(CUtensorMap* map, const void* base, int heads, i
 cudaError_t make_tmap_bf16_heads(CUtensorMap* map, const void* base, int heads, int rows,
                                  int box_heads, int head_dim = kHeadDim);
 
+// TMA descriptor for a bf16 [total, heads, head_dim] tensor with a box of
+// box_rows tokens x box_inner features of one head and a swizzle of
+// box_inner * 2 bytes (64 or 128).
+cudaError_t make_tmap_bf16_box(CUtensorMap* map, const void* base, int heads, int total, int64_t row_stride,
+                               int head_dim, int box_inner, int box_rows);
+
 // TMA descriptor for the fp32 [total, heads, 64] dq accumulator (contiguous):
 // 3-D {64, heads, total}, 128-byte swizzle, box {32, 1, 32}.
 cudaError_t make_tmap_f32_rows(CUtensorMap* map, void* base, int heads, int total);
@@ -150,6 +156,7 @@ struct FwdLaunch {
 };
 struct BwdLaunch {
   CUtensorMap q, k, v, dout, dq;
+  CUtensorMap dqo;  // bf16 dq, boxes of 32 rows x head_dim / 2 (the dq pass's TMA stores)
 };
 cudaError_t prepare_fwd(const Problem& p, FwdLaunch* l);
 cudaError_t prepare_bwd_main(const BwdProblem& p, BwdLaunch* l);
