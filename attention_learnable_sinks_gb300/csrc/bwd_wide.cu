@@ -423,40 +423,64 @@ bwd_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               }
             }
             uint32_t pP[8], pS[8];  // [2 k + rh]: block kb + k, key row rh
-            // allowed query columns [clo, clo + span) of this thread's two key
-            // rows (an empty range for rows past the end of the sequence)
-            int clo[2];
-            unsigned span[2];
-#pragma unroll
-            for (int rh = 0; rh < 2; ++rh) {
-              const int rr = 32 * quarter + 16 * grp + 8 * rh + gq;
-              const int j = u.c0 + rr;
-              clo[rh] = (p.causal ? j : 0) - qb;
-              const int chi = p.window > 0 ? j + p.window - qb : 0x40000000;
-              span[rh] = rr < u.nkeys ? (unsigned)max(chi - clo[rh], 0) : 0u;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            auto compute = [&](auto elem_tag) {
+              constexpr bool kSelect = decltype(elem_tag)::value;
+              // allowed query columns [clo, clo + span) of this thread's two key
+              // rows (an empty range for rows past the end of the sequence)
+              int clo[2];
+              unsigned span[2];
 #pragma unroll
               for (int rh = 0; rh < 2; ++rh) {
-                const int e = 4 * k + 2 * rh;
-                const float2 x = f2unpack(ffma2(f2pack(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])),
-                                                sl2x2, f2pack(a4[k].x, a4[k].y)));
-                float P0 = ex2(x.x), P1 = ex2(x.y);
-                if (kMask) {  // one unsigned compare and a select per element
-                  const int col = 8 * (kb + k) + 2 * qq;
-                  P0 = (unsigned)(col - clo[rh]) < span[rh] ? P0 : 0.f;
-                  P1 = (unsigned)(col + 1 - clo[rh]) < span[rh] ? P1 : 0.f;
+                const int rr = 32 * quarter + 16 * grp + 8 * rh + gq;
+                const int j = u.c0 + rr;
+                clo[rh] = (p.causal ? j : 0) - qb;
+                const int chi = p.window > 0 ? j + p.window - qb : 0x40000000;
+                span[rh] = rr < u.nkeys ? (unsigned)max(chi - clo[rh], 0) : 0u;
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int rh = 0; rh < 2; ++rh) {
+                  const int e = 4 * k + 2 * rh;
+                  const float2 x = f2unpack(ffma2(f2pack(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])),
+                                                  sl2x2, f2pack(a4[k].x, a4[k].y)));
+                  float P0 = ex2(x.x), P1 = ex2(x.y);
+                  if (kSelect) {  // one unsigned compare and a select per element
+                    const int col = 8 * (kb + k) + 2 * qq;
+                    P0 = (unsigned)(col - clo[rh]) < span[rh] ? P0 : 0.f;
+                    P1 = (unsigned)(col + 1 - clo[rh]) < span[rh] ? P1 : 0.f;
+                  }
+                  const uint64_t P = f2pack(P0, P1);
+                  const uint64_t t = fmul2(P, f2pack(__uint_as_float(pv[cur][e]), __uint_as_float(pv[cur][e + 1])));
+                  if (rh)
+                    sa1 = ffma2(f2pack(b2[k].x, b2[k].y), t, sa1);
+                  else
+                    sa0 = ffma2(f2pack(b2[k].x, b2[k].y), t, sa0);
+                  const float2 ds = f2unpack(ffma2(P, f2pack(a4[k].z, a4[k].w), t));  // P (dP - D)
+                  pP[2 * k + rh] = pack_bf16(P0, P1);
+                  pS[2 * k + rh] = pack_bf16(ds.x, ds.y);
                 }
-                const uint64_t P = f2pack(P0, P1);
-                const uint64_t t = fmul2(P, f2pack(__uint_as_float(pv[cur][e]), __uint_as_float(pv[cur][e + 1])));
-                if (rh)
-                  sa1 = ffma2(f2pack(b2[k].x, b2[k].y), t, sa1);
-                else
-                  sa0 = ffma2(f2pack(b2[k].x, b2[k].y), t, sa0);
-                const float2 ds = f2unpack(ffma2(P, f2pack(a4[k].z, a4[k].w), t));  // P (dP - D)
-                pP[2 * k + rh] = pack_bf16(P0, P1);
-                pS[2 * k + rh] = pack_bf16(ds.x, ds.y);
+              }
+            };
+            if constexpr (!kMask) {
+              compute(std::false_type{});
+            } else {
+              // The chunk is key rows [j0, j0 + 16) x query columns [q0, q0 + 32),
+              // the same for the whole warp. Where the band covers all of it,
+              // or none of it, no element needs its own test.
+              const int r0 = 32 * quarter + 16 * grp;
+              const int j0 = u.c0 + r0, q0 = qb + 8 * kb;
+              const bool none = r0 >= u.nkeys || (p.causal && q0 + 31 < j0) ||
+                                (p.window > 0 && q0 >= j0 + 15 + p.window);
+              const bool whole = r0 + 15 < u.nkeys && (!p.causal || q0 >= j0 + 15) &&
+                                 (p.window <= 0 || q0 + 31 < j0 + p.window);
+              if (none) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pP[e] = pS[e] = 0u;
+              } else if (whole) {
+                compute(std::false_type{});
+              } else {
+                compute(std::true_type{});
               }
             }
             // P^T (bf16 pairs) over S^T -- warp-wide: column 4 (kb + k) + qq of
