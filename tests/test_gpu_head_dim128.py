@@ -33,6 +33,9 @@ CASES = [
     ("peaked_logits", [600], 8, 1, True, 0, {"qk_std": 2.0, "sink_range": (-10.0, 10.0)}),
     ("sinks_minus30", [450], 4, 2, True, 0, {"odd_head_sink": -30.0}),
     ("several_units", [1024, 1024, 640, 1500], 16, 2, True, 0, {}),
+    ("group16", [300, 130], 16, 1, True, 0, {}),
+    ("group3", [257, 100], 6, 2, True, 0, {}),
+    ("window129", [520], 4, 1, True, 129, {}),
 ]
 
 

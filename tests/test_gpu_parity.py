@@ -27,6 +27,12 @@ SMALL = [
     ("group8", [384, 255], 16, 2, True, 0, {"sink_range": (-4.0, 4.0)}),
     ("peaked_logits", [600], 8, 1, True, 0, {"qk_std": 2.0, "sink_range": (-10.0, 10.0)}),
     ("sinks_minus30", [450], 4, 2, True, 0, {"odd_head_sink": -30.0}),
+    ("group16", [300, 130], 16, 1, True, 0, {}),
+    ("group3", [257, 100], 6, 2, True, 0, {}),
+    ("mqa64", [200], 64, 1, True, 0, {}),
+    ("mha_window", [390], 4, 4, True, 64, {}),
+    ("window127", [520], 4, 1, True, 127, {}),
+    ("window129", [520], 4, 1, True, 129, {}),
 ]
 
 
