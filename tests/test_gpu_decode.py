@@ -182,3 +182,38 @@ def make_sub(w, pick):
     """The same cache with only the picked sequences."""
     from dataclasses import replace
     return replace(w, q=w.q[pick], block_table=w.block_table[pick], seqlens=w.seqlens[pick])
+
+
+def _random_decode(i):
+    rng = np.random.default_rng(5000 + i)
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    Hkv = int(rng.integers(1, 3))
+    edges = [0, 1, 2, 127, 128, 129, 255, 256, 257]
+    lengths = [int(rng.choice(edges)) if rng.random() < 0.3 else int(rng.integers(0, 3001))
+               for _ in range(int(rng.integers(1, 6)))]
+    return dict(Hq=G * Hkv, Hkv=Hkv, lengths=lengths, bs=int(rng.choice([16, 32, 64, 128])),
+                window=int(rng.choice([0, 0, 1, 100, 128, 1000])),
+                splits=int(rng.choice([0, 0, 1, 3, 7])), d=64 if i % 2 == 0 else 128,
+                seed=6000 + i)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_decode_matches_oracle(cuda_lib, i):
+    """Seeded random draws: group size, kv heads, cache block size, lengths
+    (tile edges and empty sequences on purpose), window, split count and
+    head_dim; the split decode and the exact decode both against the oracle."""
+    c = _random_decode(i)
+    w = make_decode(f"random{i}", c["lengths"], c["Hq"], c["Hkv"], c["bs"], seed=c["seed"],
+                    window=c["window"], d=c["d"])
+    ref = run_oracle(w)
+    got = run_cuda(w, num_splits=c["splits"])
+    assert _binding.device_error(reset=True) == 0
+    assert np.all(np.isfinite(got[0]))
+    compare(w, got, ref)
+    dev = "cuda"
+    o, lse = api.decode(w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev), w.block_table.to(dev),
+                        w.seqlens.to(dev), w.sinks.to(dev), window=w.window, scale=w.scale,
+                        exact=True)
+    torch.cuda.synchronize()
+    assert _binding.device_error(reset=True) == 0
+    compare(w, (f64(o), f64(lse)), ref)
