@@ -103,9 +103,10 @@ def kernel_source_sha(kernel_file: str):
 def traffic_record(key: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, valid only while the kernel source is unchanged. ``key`` is the
-    kernel's source file, with "#deterministic" for the main backward's
-    deterministic-mode instantiation."""
-    kernel_file = key.split("#")[0]
+    kernel's source file, then "@<workload>" for a workload other than dense,
+    then "#deterministic" for the main backward's deterministic-mode
+    instantiation or "#exact" for the forward kernel's decode form."""
+    kernel_file = key.split("#")[0].split("@")[0]
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -662,6 +663,10 @@ def run_decode(args):
 
     peaks, peak_src = load_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # counters of the decode's dominant kernel: the split kernel, or the
+    # forward kernel's decode form for the exact decode
+    tr = traffic_record(f"fwd.cu@{args.workload}#exact" if args.decode_exact
+                        else f"decode.cu@{args.workload}")
     line = {
         "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -674,7 +679,8 @@ def run_decode(args):
         "roofline": {"bound": "hbm", "kernel": "decode (split + combine)", "achieved": value / world,
                      "peak": hbm, "unit": "GB/s", "frac": value / world / hbm,
                      "peak_source": f"{peak_src} HBM copy",
-                     "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K},
         "gpu_launches": launches,
