@@ -5,6 +5,7 @@ package is its thin PyTorch binding. Importing the package does not load the
 library; the first call does, and raises if it is missing.
 """
 
-from .api import backward, decode, forward, sink_attention, workspace_bytes  # noqa: F401
+from .api import (SinkAttention, backward, decode, forward, sink_attention,  # noqa: F401
+                  workspace_bytes)
 
-__all__ = ["sink_attention", "forward", "backward", "workspace_bytes"]
+__all__ = ["SinkAttention", "sink_attention", "forward", "backward", "decode", "workspace_bytes"]

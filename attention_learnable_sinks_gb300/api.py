@@ -261,6 +261,29 @@ def sink_attention(q, k, v, sinks=None, cu_seqlens=None, max_seqlen=None, *, cau
     return o.reshape(B, T, *o.shape[1:]) if batched else o
 
 
+class SinkAttention(torch.nn.Module):
+    """The sink-attention layer with its sinks as a parameter: one fp32 logit
+    per query head (``init`` everywhere at the start), trained like any
+    other weight. ``forward(q, k, v, cu_seqlens=None, max_seqlen=None)``
+    takes the shapes ``sink_attention`` takes and returns O."""
+
+    def __init__(self, num_heads: int, *, causal: bool = True, window: int = 0, scale=None,
+                 deterministic: bool = False, init: float = 0.0, device=None):
+        super().__init__()
+        self.sinks = torch.nn.Parameter(torch.full((num_heads,), float(init), dtype=torch.float32,
+                                                   device=device))
+        self.causal, self.window, self.scale = causal, window, scale
+        self.deterministic = deterministic
+
+    def forward(self, q, k, v, cu_seqlens=None, max_seqlen=None):
+        return sink_attention(q, k, v, self.sinks, cu_seqlens, max_seqlen, causal=self.causal,
+                              window=self.window, scale=self.scale, deterministic=self.deterministic)
+
+    def extra_repr(self) -> str:
+        return (f"num_heads={self.sinks.numel()}, causal={self.causal}, window={self.window}, "
+                f"deterministic={self.deterministic}")
+
+
 def _split_sequences(lens, causal: bool, window: int, groups: int):
     """Boundaries (sequence indices) of up to ``groups`` runs of consecutive
     sequences with about equal attention cost (allowed pairs)."""

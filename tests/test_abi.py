@@ -257,3 +257,13 @@ def test_decode_workspace_size():
     assert lib.sinkattn_decode_workspace_size(64, 64, 0) == 0
     assert lib.sinkattn_decode_workspace_size(64, 64, 65) == 0
     assert lib.sinkattn_decode_workspace_size(-1, 64, 1) == 0
+
+
+def test_module_holds_one_fp32_sink_per_head():
+    import torch
+    from attention_learnable_sinks_gb300 import SinkAttention
+    layer = SinkAttention(12, window=64, init=-1.5)
+    assert [n for n, _ in layer.named_parameters()] == ["sinks"]
+    assert layer.sinks.shape == (12,) and layer.sinks.dtype == torch.float32
+    assert bool((layer.sinks == -1.5).all()) and layer.sinks.requires_grad
+    assert "num_heads=12" in repr(layer) and "window=64" in repr(layer)

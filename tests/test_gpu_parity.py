@@ -103,6 +103,29 @@ def test_autograd_op_matches_oracle(cuda_lib):
     assert_dsinks(f64(s.grad), ref["dsinks"], cond)
 
 
+def test_module_with_sink_parameter_matches_oracle(cuda_lib):
+    """SinkAttention holds the sinks as a parameter; its gradient after one
+    backward is dL/dS_h, and an optimizer step moves it."""
+    w = make("module", [300, 77], 8, 2, seed=12, window=100)
+    layer = api.SinkAttention(8, window=100, device="cuda")
+    with torch.no_grad():
+        layer.sinks.copy_(w.sinks)
+    q = w.q.cuda().requires_grad_()
+    k = w.k.cuda().requires_grad_()
+    v = w.v.cuda().requires_grad_()
+    o = layer(q, k, v, w.cu_seqlens.cuda(), w.max_seqlen)
+    o.backward(w.dout.cuda())
+    ref, *_ = run_oracle(w)
+    from parity import assert_close, f64
+    for n, t in (("o", o), ("dq", q.grad), ("dk", k.grad), ("dv", v.grad)):
+        assert_close(n, f64(t), ref[n])
+    cond = dsink_condition(w.sinks.numpy().astype(np.float64), ref["lse"], ref["o"], ref["_do"])
+    assert_dsinks(f64(layer.sinks.grad), ref["dsinks"], cond)
+    before = layer.sinks.detach().clone()
+    torch.optim.SGD(layer.parameters(), lr=0.1).step()
+    assert torch.allclose(layer.sinks.detach(), before - 0.1 * layer.sinks.grad)
+
+
 def test_batched_4d_layout(cuda_lib):
     w = make("batched", [200, 200], 4, 2, seed=11)
     q = w.q.cuda().view(2, 200, 4, 64)
