@@ -1,5 +1,5 @@
-"""Multi-rank layouts on CPU ranks (gloo, world size 2), with the fp64 oracle
-standing in for the kernels on each rank.
+"""Multi-rank layouts on CPU ranks (gloo, world sizes 2 to 4), with the fp64
+oracle standing in for the kernels on each rank.
 
 * Data parallel: the batch's sequences are split by attention cost; each rank
   computes its sequences and the per-head sink gradients are summed with one
@@ -25,7 +25,6 @@ import oracle
 from attention_learnable_sinks_gb300 import sharding
 from attention_learnable_sinks_gb300.workloads import make
 
-WORLD = 2
 ALL = ("o", "lse", "dq", "dk", "dv", "dsinks")
 
 
@@ -35,9 +34,9 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _workload(d=64):
-    # ragged lengths, an empty and a length-1 sequence, GQA 4:1, W = 2 head shards
-    return make("multirank", [150, 37, 0, 260, 1, 90], 8, 2, seed=41, sink_range=(-3.0, 3.0), d=d)
+def _workload(d=64, hkv=2):
+    # ragged lengths, an empty and a length-1 sequence, GQA 8:hkv
+    return make("multirank", [150, 37, 0, 260, 1, 90], 8, hkv, seed=41, sink_range=(-3.0, 3.0), d=d)
 
 
 def _f64(t):
@@ -65,14 +64,14 @@ def _reference(w):
                            want=ALL, nthreads=2)
 
 
-def _spawn(fn, *args):
+def _spawn(fn, world, *args):
     port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.SimpleQueue()
-    procs = [ctx.Process(target=_entry, args=(fn, r, port, q, *args)) for r in range(WORLD)]
+    procs = [ctx.Process(target=_entry, args=(fn, r, world, port, q, *args)) for r in range(world)]
     for p in procs:
         p.start()
-    results = [q.get() for _ in range(WORLD)]
+    results = [q.get() for _ in range(world)]
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0, f"rank process exited with {p.exitcode}"
@@ -81,13 +80,13 @@ def _spawn(fn, *args):
     return sorted(results, key=lambda r: r["rank"])
 
 
-def _entry(fn, rank, port, q, *args):
+def _entry(fn, rank, world, port, q, *args):
     import traceback
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     try:
-        dist.init_process_group("gloo", rank=rank, world_size=WORLD)
-        q.put(fn(rank, *args))
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        q.put(fn(rank, world, *args))
     except Exception:
         q.put(f"rank {rank}:\n{traceback.format_exc()}")
     finally:
@@ -95,10 +94,10 @@ def _entry(fn, rank, port, q, *args):
             dist.destroy_process_group()
 
 
-def _rank_data_parallel(rank, d=64):
+def _rank_data_parallel(rank, world, d=64):
     w = _workload(d)
     lens = (w.cu_seqlens[1:] - w.cu_seqlens[:-1]).tolist()
-    parts = sharding.partition_sequences(lens, WORLD, w.causal, w.window)
+    parts = sharding.partition_sequences(lens, world, w.causal, w.window)
     tok, cu, maxlen = sharding.shard_tokens(w.cu_seqlens.tolist(), parts[rank])
     q, k, v, do = (_f64(t[tok]) for t in (w.q, w.k, w.v, w.dout))
     r = oracle.sinkattn(q, k, v, _f64(w.sinks), cu.numpy(), causal=w.causal, window=w.window,
@@ -109,11 +108,11 @@ def _rank_data_parallel(rank, d=64):
     return {"rank": rank, "tok": tok.numpy(), "seqs": parts[rank], **r}
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_data_parallel_split_matches_whole_batch(d):
+@pytest.mark.parametrize("world, d", [(2, 64), (2, 128), (3, 64), (4, 64)])
+def test_data_parallel_split_matches_whole_batch(world, d):
     w = _workload(d)
     ref = _reference(w)
-    res = _spawn(_rank_data_parallel, d)
+    res = _spawn(_rank_data_parallel, world, d)
     seen = sorted(b for r in res for b in r["seqs"])
     assert seen == list(range(w.nseq)), "every sequence on exactly one rank"
     for r in res:
@@ -127,10 +126,10 @@ def test_data_parallel_split_matches_whole_batch(d):
     assert not np.allclose(res[0]["dsinks"], ref["dsinks"])
 
 
-def _rank_head_split(rank, d=64):
+def _rank_head_split(rank, world, d=64, hkv=2):
     import torch.distributed as dist
-    w = _workload(d)
-    splits = sharding.token_split(w.total, WORLD)
+    w = _workload(d, hkv)
+    splits = sharding.token_split(w.total, world)
     t0 = sum(splits[:rank])
     sl = slice(t0, t0 + splits[rank])
     q, k, v, do = (torch.from_numpy(_f64(t[sl])) for t in (w.q, w.k, w.v, w.dout))
@@ -151,12 +150,13 @@ def _rank_head_split(rank, d=64):
             bool((ds.numpy()[np.r_[0:hs.start, hs.stop:w.Hq]] == 0).all())}
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_head_split_all_to_all_matches_single_process(d):
-    w = _workload(d)
+@pytest.mark.parametrize("world, d, hkv", [(2, 64, 2), (2, 128, 2), (4, 64, 4)])
+def test_head_split_all_to_all_matches_single_process(world, d, hkv):
+    w = _workload(d, hkv)
     ref = _reference(w)
-    res = _spawn(_rank_head_split, d)
-    assert [r["slice"] for r in res] == [(0, 269), (269, 538)]
+    res = _spawn(_rank_head_split, world, d, hkv)
+    bounds = np.cumsum([0] + sharding.token_split(w.total, world))
+    assert [r["slice"] for r in res] == [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:])]
     for r in res:
         a, b = r["slice"]
         for name in ("o", "dq", "dk", "dv"):
