@@ -130,8 +130,8 @@ def backward(q, k, v, sinks, cu_seqlens, max_seqlen, o, lse, dout, *, causal=Tru
     dv = dv if dv is not None else torch.empty(total, Hkv, d, dtype=torch.bfloat16, device=q.device)
     if sinks is not None and dsinks is None:
         dsinks = torch.empty(Hq, dtype=torch.float32, device=q.device)
-    nbytes = L.sinkattn_bwd_workspace_size(nseq, total, Hq, Hkv, d)
-    if workspace is None:
+    if workspace is None:  # sized for the mode: the deterministic backward has no dq accumulator
+        nbytes = L.sinkattn_bwd_workspace_size_mode(nseq, total, Hq, Hkv, d, 1 if deterministic else 0)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     p = BwdParams()
     _fill_fwd(p.fwd, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, scale, o, lse)
